@@ -1,0 +1,217 @@
+/*
+ * nvfp4_skinny.h -- C ABI of the GB300 (sm_103a) NVFP4 W4A16 skinny decode library.
+ *
+ * What it computes (sources are the pages' titles and sections):
+ *
+ *   NVFP4 weight: w_hat[n,k] = e2m1(q[n,k]) * e4m3(s[n, k/16]) * g          (1)
+ *     "E2M1 weights + E4M3 group-16 scales + FP32 global" -- gemma-cuda-hybrid
+ *     README, "Everything it has / Inference engine"; the offline repack into
+ *     MMA-fragment order -- same page, "Why it's NVIDIA-only ... /
+ *     NVFP4-specific".
+ *   Skinny GEMM: y[m,n] = sum_k w_hat[n,k] * x[m,k], M <= 16, fp32
+ *     accumulate, bf16 in and out -- gemma-cuda-hybrid README, "Everything it
+ *     has / Inference engine" (the tensor-core GEMM for all M<=16 GEMMs).
+ *   MoE FFN: router top-k over the logits, softmax over the chosen k, grouped
+ *     gate+up product, h = gelu_tanh(gate) * up, grouped down product,
+ *     probability-weighted sum plus the always-on shared expert --
+ *     TensorSharp docs/models/gemma4.md, "3.1 Per-layer (dense)", "3.2
+ *     Per-layer (MoE)", "4.6 MoE", "14. Optimization opportunities / Completed
+ *     (Expert-batched FFN)"; GELU-tanh -- TensorFold issue #1048, "Steps",
+ *     step 2; "Grouped weight-resident MoE (no atomics ...)" -- gemma-cuda-hybrid
+ *     README, "Everything it has / Inference engine".
+ *   lm_head + greedy argmax: per token row the largest logit of W_hat . x and
+ *     its lowest index, no logits written to memory -- gemma-cuda-hybrid
+ *     README, "Headline numbers" (bit-exact greedy) and "Everything it has"
+ *     (NVFP4 tied lm_head).
+ *
+ * Conventions for every call:
+ *   - Pointers marked (device) are CUDA device pointers; (host) are host
+ *     pointers.  The caller owns every buffer; the library allocates no memory
+ *     on any call.
+ *   - Device work is enqueued asynchronously on `stream` (0 = legacy default
+ *     stream).  Arguments are checked on the host before anything is launched;
+ *     a bad argument returns an error status and launches nothing.  A launch
+ *     failure returns NVFP4_ERR_CUDA (the CUDA error is left for
+ *     cudaGetLastError()).  No C++ exception crosses this boundary.
+ *   - bf16 tensors are passed as uint16_t bit patterns, row-major, contiguous.
+ *   - Preconditions not checked on the device: inputs are finite; expert ids
+ *     passed to moe_ffn_grouped come from moe_route_topk; workspaces are not
+ *     shared by calls that may run concurrently.
+ *   - Kernel waits are bounded (about one second); a wait that runs out sets a
+ *     bit in a device error word read by nvfp4_device_error().
+ */
+#ifndef NVFP4_SKINNY_H_
+#define NVFP4_SKINNY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NVFP4_LAYOUT_VERSION 1u
+
+/* Flags of an nvfp4_weight / nvfp4_repack call. */
+#define NVFP4_GATED 1u /* rows are [gate (N/2) || up (N/2)], N/2 % 8 == 0 */
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_NULL = 1,      /* a required pointer is NULL */
+  NVFP4_ERR_SHAPE = 2,     /* a size is out of range or inconsistent */
+  NVFP4_ERR_ALIGN = 3,     /* a pointer is not aligned as documented */
+  NVFP4_ERR_WORKSPACE = 4, /* workspace NULL or smaller than *_workspace_bytes() */
+  NVFP4_ERR_LAYOUT = 5,    /* nvfp4_weight.layout_version or flags mismatch */
+  NVFP4_ERR_CUDA = 6       /* a CUDA launch or query failed */
+} nvfp4_status;
+
+/*
+ * A repacked NVFP4 weight (a view; the caller owns the memory).
+ *   data          (device) repacked bytes, nvfp4_repacked_bytes(n, k, num_matrices)
+ *                 long, 16-byte aligned, written by nvfp4_repack().
+ *   global_scale  (device) fp32 [num_matrices]: g of formula (1) per matrix.
+ *   n, k          logical rows and columns of one matrix; k % 16 == 0.
+ *   num_matrices  1, or E for a stack of E expert matrices [E, n, k].
+ *   flags         NVFP4_GATED for a fused [gate || up] matrix, else 0;
+ *                 must equal the flags given to nvfp4_repack().
+ *   layout_version  NVFP4_LAYOUT_VERSION.
+ *
+ * Repacked layout (version 1): rows padded to a multiple of 16 and columns to a
+ * multiple of 64 with zero bytes; a gated matrix first moves gate row i to row
+ * 16*(i/8) + i%8 and up row i to 16*(i/8) + 8 + i%8.  The padded matrix is cut
+ * into 576-byte tiles of 16 rows x 64 columns, row-block major.  In a tile,
+ * byte 16*lane + 4*kt + r (lane = 4*g + t) holds columns c, c+1 of row
+ * 16*rb + g + 8*(r&1) with c = 64*kc + 16*kt + 2*t + 8*(r>>1) (low nibble =
+ * column c), and byte 512 + 8*g + 2*kt + h holds the scale of row
+ * 16*rb + g + 8*h, group 4*kc + kt: one 16-byte load per lane gives an m16n8k16
+ * A fragment for four 16-column groups.  Scale codes are stored with their sign
+ * bit clear: a negative scale is folded into the signs of its 16 elements.
+ */
+typedef struct {
+  const void *data;
+  const float *global_scale;
+  int32_t n;
+  int32_t k;
+  int32_t num_matrices;
+  uint32_t flags;
+  uint32_t layout_version;
+} nvfp4_weight;
+
+/* Human-readable name of a status code (static string). */
+const char *nvfp4_status_string(nvfp4_status st);
+
+/* Library's repacked-layout version (NVFP4_LAYOUT_VERSION at build time). */
+uint32_t nvfp4_layout_version(void);
+
+/*
+ * Device error word: bit 0 = a kernel's bounded wait ran out of time.  Reads
+ * the word (synchronously, on the current device) into *out and clears it if
+ * `clear` is nonzero.
+ */
+nvfp4_status nvfp4_device_error(uint32_t *out, int32_t clear);
+
+/* Bytes of a repacked weight of num_matrices x [n, k] (0 for invalid sizes). */
+size_t nvfp4_repacked_bytes(int32_t n, int32_t k, int32_t num_matrices);
+
+/*
+ * Offline quantizer (formula (1) in reverse), deciding in IEEE fp32:
+ *   g = amax|W| / 2688; per 16-group t = (bmax / 6) / g, scale = E4M3
+ *   round-to-nearest-even saturating at 448; element = E2M1
+ *   round-to-nearest-even saturating at 6 of w / (e4m3(scale) * g); a group
+ *   whose scale is 0 gets zero codes; an all-zero matrix gets g = 0.
+ *   w        (device) fp32 [num_matrices, n, k], k % 16 == 0.
+ *   nibbles  (device) u8 [num_matrices, n, k/2], canonical: column 2i in the
+ *            low nibble of byte i.
+ *   scales   (device) u8 [num_matrices, n, k/16].
+ *   global_scale (device) fp32 [num_matrices].
+ *   ws       (device) nvfp4_quantize_workspace_bytes(num_matrices) bytes.
+ */
+size_t nvfp4_quantize_workspace_bytes(int32_t num_matrices);
+nvfp4_status nvfp4_quantize(const float *w, int32_t num_matrices, int32_t n, int32_t k, uint8_t *nibbles,
+                            uint8_t *scales, float *global_scale, void *ws, size_t ws_bytes,
+                            cudaStream_t stream);
+
+/*
+ * Offline repack of canonical NVFP4 bytes into the kernel layout above.
+ *   nibbles, scales (device) canonical, as written by nvfp4_quantize().
+ *   out      (device) nvfp4_repacked_bytes(n, k, num_matrices) bytes, 16-byte
+ *            aligned; every byte is written (padding with zeros).
+ *   flags    0 or NVFP4_GATED (then n % 16 == 0).
+ */
+nvfp4_status nvfp4_repack(const uint8_t *nibbles, const uint8_t *scales, int32_t num_matrices, int32_t n,
+                          int32_t k, uint32_t flags, void *out, cudaStream_t stream);
+
+/*
+ * Dense skinny GEMM: y[m, :] = bf16( W_hat . x[m, :] ), 1 <= m <= 16.
+ *   w   num_matrices == 1, flags == 0.
+ *   x   (device) bf16 [m, w->k], 16-byte aligned.
+ *   y   (device) bf16 [m, w->n], 4-byte aligned.
+ *   ws  (device) nvfp4_gemm_workspace_bytes(m, n, k) bytes, 16-byte aligned
+ *       (may be NULL when that is 0).  Its first 4 KiB hold arrival counters
+ *       that must be zero before the first call that uses this workspace (for
+ *       example cudaMemsetAsync once after allocation); every call leaves them
+ *       consistent for the next.
+ * M = 1..7 runs on CUDA cores (warp-shuffle reduction); M = 8..16 on m16n8k16
+ * tensor-core MMAs with the weights as the 16-row operand.
+ */
+size_t nvfp4_gemm_workspace_bytes(int32_t m, int32_t n, int32_t k);
+nvfp4_status nvfp4_gemm(const nvfp4_weight *w, const uint16_t *x, int32_t m, uint16_t *y, void *ws,
+                        size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * MoE router: per token m, the top_k largest logits (descending; equal logits
+ * -> lower expert id) and a softmax over those top_k logits; then a stable
+ * grouping of the m*top_k (token, slot) pairs by expert with no atomics.
+ *   logits          (device) fp32 [m, n_experts]
+ *   ids             (device) int32 [m, top_k]
+ *   probs           (device) fp32 [m, top_k]
+ *   expert_offsets  (device) int32 [n_experts + 1]: expert e's pairs are
+ *                   sorted_pairs[offsets[e] .. offsets[e+1]).
+ *   sorted_pairs    (device) int32 [m * top_k]: pair index p = token*top_k + slot,
+ *                   ascending within an expert.
+ * Limits: 1 <= m <= 4096, 1 <= top_k <= 32, top_k <= n_experts <= 1024,
+ * m * top_k <= 16384.
+ */
+nvfp4_status moe_route_topk(const float *logits, int32_t m, int32_t n_experts, int32_t top_k, int32_t *ids,
+                            float *probs, int32_t *expert_offsets, int32_t *sorted_pairs,
+                            cudaStream_t stream);
+
+/*
+ * Grouped MoE FFN: out[t] = bf16( sum_r probs[t,r] * down_e(h_{t,r}) + shared_down(h_{t,shared}) )
+ * with h = bf16( gelu_tanh(gate_e . x_t) * (up_e . x_t) ) and e = ids[t, r].
+ *   x               (device) bf16 [m, d], 16-byte aligned.
+ *   probs, expert_offsets, sorted_pairs: as written by moe_route_topk.
+ *   gate_up         stacked [E, 2*inter, d], flags NVFP4_GATED.
+ *   down            stacked [E, d, inter], flags 0.
+ *   shared_gate_up, shared_down: one matrix each of the same shapes, or both NULL.
+ *   out             (device) bf16 [m, d].
+ *   ws              (device) moe_ffn_workspace_bytes(m, top_k, d, inter) bytes.
+ * Limits: 1 <= m <= 4096, d % 64 == 0, inter % 64 == 0.
+ */
+size_t moe_ffn_workspace_bytes(int32_t m, int32_t top_k, int32_t d, int32_t inter);
+nvfp4_status moe_ffn_grouped(const uint16_t *x, int32_t m, int32_t top_k, const float *probs,
+                             const int32_t *expert_offsets, const int32_t *sorted_pairs,
+                             const nvfp4_weight *gate_up, const nvfp4_weight *down,
+                             const nvfp4_weight *shared_gate_up, const nvfp4_weight *shared_down,
+                             uint16_t *out, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * lm_head with fused greedy argmax: for each token row m, max_n (W_hat . x_m)[n]
+ * in fp32 and the lowest n reaching it.  The vocabulary is split across CTAs
+ * and K across the warps of a CTA; no logits are written to memory.
+ *   w          num_matrices == 1, flags == 0 (n = vocabulary size).
+ *   x          (device) bf16 [m, w->k], 1 <= m <= 16, 16-byte aligned.
+ *   max_logit  (device) fp32 [m];  argmax (device) int32 [m].
+ *   ws         (device) lm_head_workspace_bytes(m, n) bytes, 8-byte aligned.
+ */
+size_t lm_head_workspace_bytes(int32_t m, int32_t vocab);
+nvfp4_status lm_head_argmax(const nvfp4_weight *w, const uint16_t *x, int32_t m, float *max_logit,
+                            int32_t *argmax, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_SKINNY_H_ */

@@ -1,0 +1,238 @@
+"""Thin Python binding over the C ABI of ``libnvfp4skinny.so`` (ctypes).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  PyTorch supplies device memory and streams.  There is
+no fallback: if the shared library is missing, ``load()`` raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from .build import LIB
+
+NVFP4_GATED = 1
+LAYOUT_VERSION = 1
+
+STATUS = {0: "ok", 1: "null pointer", 2: "bad shape", 3: "misaligned pointer",
+          4: "workspace missing or too small", 5: "weight layout version or flags mismatch", 6: "CUDA error"}
+
+EXPORTS = (
+    "nvfp4_status_string", "nvfp4_layout_version", "nvfp4_device_error", "nvfp4_repacked_bytes",
+    "nvfp4_quantize_workspace_bytes", "nvfp4_quantize", "nvfp4_repack", "nvfp4_gemm_workspace_bytes",
+    "nvfp4_gemm", "moe_route_topk", "moe_ffn_workspace_bytes", "moe_ffn_grouped",
+    "lm_head_workspace_bytes", "lm_head_argmax",
+)
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, call: str, status: int):
+        super().__init__(f"{call} failed: {STATUS.get(status, status)} ({status})")
+        self.status = status
+
+
+class CWeight(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("global_scale", ctypes.c_void_p), ("n", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("num_matrices", ctypes.c_int32), ("flags", ctypes.c_uint32),
+                ("layout_version", ctypes.c_uint32)]
+
+
+@dataclass
+class Weight:
+    """A repacked NVFP4 weight living on the GPU (owns its tensors)."""
+    data: torch.Tensor          # uint8, repacked tiles
+    global_scale: torch.Tensor  # float32 [num_matrices]
+    n: int
+    k: int
+    num_matrices: int = 1
+    flags: int = 0
+
+    def c(self) -> CWeight:
+        return CWeight(self.data.data_ptr(), self.global_scale.data_ptr(), self.n, self.k,
+                       self.num_matrices, self.flags, LAYOUT_VERSION)
+
+    @property
+    def nbytes_algorithmic(self) -> int:
+        """Bytes the method must read: n*k/2 nibbles + n*k/16 scales per matrix."""
+        return self.num_matrices * (self.n * self.k // 2 + self.n * self.k // 16)
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_SZ = ctypes.c_size_t
+
+
+def _sig(lib):
+    lib.nvfp4_status_string.restype = ctypes.c_char_p
+    lib.nvfp4_status_string.argtypes = [ctypes.c_int]
+    lib.nvfp4_layout_version.restype = ctypes.c_uint32
+    lib.nvfp4_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), _I]
+    lib.nvfp4_repacked_bytes.restype = _SZ
+    lib.nvfp4_repacked_bytes.argtypes = [_I, _I, _I]
+    lib.nvfp4_quantize_workspace_bytes.restype = _SZ
+    lib.nvfp4_quantize_workspace_bytes.argtypes = [_I]
+    lib.nvfp4_quantize.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]
+    lib.nvfp4_repack.argtypes = [_P, _P, _I, _I, _I, ctypes.c_uint32, _P, _P]
+    lib.nvfp4_gemm_workspace_bytes.restype = _SZ
+    lib.nvfp4_gemm_workspace_bytes.argtypes = [_I, _I, _I]
+    lib.nvfp4_gemm.argtypes = [ctypes.POINTER(CWeight), _P, _I, _P, _P, _SZ, _P]
+    lib.moe_route_topk.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P]
+    lib.moe_ffn_workspace_bytes.restype = _SZ
+    lib.moe_ffn_workspace_bytes.argtypes = [_I, _I, _I, _I]
+    lib.moe_ffn_grouped.argtypes = [_P, _I, _I, _P, _P, _P, ctypes.POINTER(CWeight), ctypes.POINTER(CWeight),
+                                    ctypes.POINTER(CWeight), ctypes.POINTER(CWeight), _P, _P, _SZ, _P]
+    lib.lm_head_workspace_bytes.restype = _SZ
+    lib.lm_head_workspace_bytes.argtypes = [_I, _I]
+    lib.lm_head_argmax.argtypes = [ctypes.POINTER(CWeight), _P, _I, _P, _P, _P, _SZ, _P]
+    for name in ("nvfp4_quantize", "nvfp4_repack", "nvfp4_gemm", "moe_route_topk", "moe_ffn_grouped",
+                 "lm_head_argmax", "nvfp4_device_error"):
+        getattr(lib, name).restype = ctypes.c_int
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+class Library:
+    """The loaded C ABI; methods take CUDA tensors and enqueue on the current stream."""
+
+    def __init__(self, path: str = LIB):
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with `python -m nvfp4_w4a16_moe_skinny_gb300.build` "
+                               "(there is no CPU fallback)")
+        self.path = path
+        self.lib = ctypes.CDLL(path)
+        _sig(self.lib)
+        self._ws = {}
+
+    # -------------------------------------------------------------- plumbing
+    def _check(self, call, st):
+        if st != 0:
+            raise NVFP4Error(call, st)
+
+    def workspace(self, key, nbytes: int, device) -> torch.Tensor:
+        """A per-(call kind, device) workspace, zero-filled once at allocation."""
+        cur = self._ws.get((key, device))
+        if cur is None or cur.numel() < nbytes:
+            cur = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device)
+            self._ws[(key, device)] = cur
+        return cur
+
+    def device_error(self, clear: bool = True) -> int:
+        v = ctypes.c_uint32(0)
+        self._check("nvfp4_device_error", self.lib.nvfp4_device_error(ctypes.byref(v), int(clear)))
+        return v.value
+
+    def repacked_bytes(self, n, k, num_matrices=1) -> int:
+        return self.lib.nvfp4_repacked_bytes(n, k, num_matrices)
+
+    # -------------------------------------------------------------- offline
+    def quantize(self, w: torch.Tensor, stream=None):
+        """fp32 [E, n, k] or [n, k] on the GPU -> canonical (nibbles, scales, global_scale)."""
+        squeeze = w.dim() == 2
+        w3 = w.unsqueeze(0) if squeeze else w
+        w3 = w3.contiguous()
+        e, n, k = w3.shape
+        nib = torch.empty((e, n, k // 2), dtype=torch.uint8, device=w.device)
+        sc = torch.empty((e, n, k // 16), dtype=torch.uint8, device=w.device)
+        g = torch.empty((e,), dtype=torch.float32, device=w.device)
+        ws = torch.empty((max(1, self.lib.nvfp4_quantize_workspace_bytes(e)),), dtype=torch.uint8, device=w.device)
+        self._check("nvfp4_quantize", self.lib.nvfp4_quantize(
+            w3.data_ptr(), e, n, k, nib.data_ptr(), sc.data_ptr(), g.data_ptr(), ws.data_ptr(), ws.numel(),
+            _stream(stream)))
+        if squeeze:
+            return nib[0], sc[0], g
+        return nib, sc, g
+
+    def repack(self, nib: torch.Tensor, sc: torch.Tensor, gscale: torch.Tensor, gated: bool = False,
+               stream=None) -> Weight:
+        nib3 = nib.unsqueeze(0) if nib.dim() == 2 else nib
+        sc3 = sc.unsqueeze(0) if sc.dim() == 2 else sc
+        e, n, kh = nib3.shape
+        k = 2 * kh
+        out = torch.empty((self.repacked_bytes(n, k, e),), dtype=torch.uint8, device=nib.device)
+        flags = NVFP4_GATED if gated else 0
+        self._check("nvfp4_repack", self.lib.nvfp4_repack(
+            nib3.contiguous().data_ptr(), sc3.contiguous().data_ptr(), e, n, k, flags, out.data_ptr(),
+            _stream(stream)))
+        return Weight(out, gscale.reshape(-1).contiguous().float(), n, k, e, flags)
+
+    def prepare(self, w: torch.Tensor, gated: bool = False, stream=None) -> Weight:
+        """quantize + repack of fp32 weights already on the GPU."""
+        nib, sc, g = self.quantize(w, stream)
+        return self.repack(nib, sc, g, gated, stream)
+
+    # -------------------------------------------------------------- hot path
+    def gemm(self, w: Weight, x: torch.Tensor, y: torch.Tensor = None, stream=None) -> torch.Tensor:
+        m = x.shape[0]
+        if y is None:
+            y = torch.empty((m, w.n), dtype=torch.bfloat16, device=x.device)
+        nbytes = self.lib.nvfp4_gemm_workspace_bytes(m, w.n, w.k)
+        ws = self.workspace("gemm", nbytes, x.device)
+        cw = w.c()
+        self._check("nvfp4_gemm", self.lib.nvfp4_gemm(
+            ctypes.byref(cw), x.data_ptr(), m, y.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
+        return y
+
+    def lm_head_argmax(self, w: Weight, x: torch.Tensor, out=None, stream=None):
+        m = x.shape[0]
+        if out is None:
+            out = (torch.empty((m,), dtype=torch.float32, device=x.device),
+                   torch.empty((m,), dtype=torch.int32, device=x.device))
+        nbytes = self.lib.lm_head_workspace_bytes(m, w.n)
+        ws = self.workspace("lm_head", nbytes, x.device)
+        cw = w.c()
+        self._check("lm_head_argmax", self.lib.lm_head_argmax(
+            ctypes.byref(cw), x.data_ptr(), m, out[0].data_ptr(), out[1].data_ptr(), ws.data_ptr(), ws.numel(),
+            _stream(stream)))
+        return out
+
+    def route_topk(self, logits: torch.Tensor, top_k: int, out=None, stream=None):
+        m, e = logits.shape
+        if out is None:
+            dev = logits.device
+            out = (torch.empty((m, top_k), dtype=torch.int32, device=dev),
+                   torch.empty((m, top_k), dtype=torch.float32, device=dev),
+                   torch.empty((e + 1,), dtype=torch.int32, device=dev),
+                   torch.empty((m * top_k,), dtype=torch.int32, device=dev))
+        ids, probs, offsets, pairs = out
+        self._check("moe_route_topk", self.lib.moe_route_topk(
+            logits.data_ptr(), m, e, top_k, ids.data_ptr(), probs.data_ptr(), offsets.data_ptr(), pairs.data_ptr(),
+            _stream(stream)))
+        return out
+
+    def moe_ffn(self, x, top_k, probs, offsets, pairs, gate_up: Weight, down: Weight, shared_gate_up: Weight = None,
+                shared_down: Weight = None, out=None, stream=None):
+        m, d = x.shape
+        inter = down.k
+        if out is None:
+            out = torch.empty((m, d), dtype=torch.bfloat16, device=x.device)
+        nbytes = self.lib.moe_ffn_workspace_bytes(m, top_k, d, inter)
+        ws = self.workspace("moe", nbytes, x.device)
+        cg, cd = gate_up.c(), down.c()
+        sg = ctypes.byref(shared_gate_up.c()) if shared_gate_up is not None else None
+        sd = ctypes.byref(shared_down.c()) if shared_down is not None else None
+        self._check("moe_ffn_grouped", self.lib.moe_ffn_grouped(
+            x.data_ptr(), m, top_k, probs.data_ptr(), offsets.data_ptr(), pairs.data_ptr(), ctypes.byref(cg),
+            ctypes.byref(cd), sg, sd, out.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
+        return out
+
+
+_LIB = None
+
+
+def load(path: str = LIB) -> Library:
+    global _LIB
+    if _LIB is None or _LIB.path != path:
+        _LIB = Library(path)
+    return _LIB

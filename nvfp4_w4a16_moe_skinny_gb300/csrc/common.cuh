@@ -1,0 +1,221 @@
+// Device helpers shared by the NVFP4 skinny kernels (sm_103a only).
+//
+// Inline PTX for: mbarriers with bounded waits, 1-D bulk copies (TMA engine)
+// global -> shared with an L2 evict-first hint, the hardware E2M1/E4M3
+// converters, and the m16n8k16 f16 tensor-core MMA.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "nvfp4_skinny.h"
+
+namespace nvfp4 {
+
+constexpr int kTileRows = 16;       // rows per repacked tile
+constexpr int kTileK = 64;          // K columns per repacked tile
+constexpr int kTileBytes = 576;     // 512 B of nibbles + 64 B of scales
+constexpr int kTileNibBytes = 512;
+
+// Error word shared by all kernels of the library (read by nvfp4_device_error()).
+// Bit 0: an mbarrier wait ran out of time.  The library is one translation
+// unit, so this header is included exactly once.
+__device__ unsigned int g_device_error = 0;
+
+constexpr unsigned kErrWaitTimeout = 1u;
+// ~1 s at 2 GHz: far above any legitimate wait for a bulk copy.
+constexpr long long kWaitCycles = 2000000000ll;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded warp-collective wait (all 32 lanes call it) for the phase with the
+// given parity to complete.  Every lane observes the completion itself (so the
+// bulk-copied bytes are visible to it) and all lanes return the same answer:
+// false, with kErrWaitTimeout recorded, if the phase did not complete within
+// kWaitCycles.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    if (__any_sync(0xffffffffu, clock64() - t0 > kWaitCycles)) {
+      if ((threadIdx.x & 31) == 0) atomicOr(&g_device_error, kErrWaitTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 1-D bulk copy global -> shared (TMA engine); completion is counted on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// Four E2M1 pairs (the four bytes of w) -> four f16x2 (low nibble -> low half).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+// Scale byte j of `w` (an E4M3 code with its sign bit clear) as an f16x2 with
+// the value in both halves, times 2^-8: the code's 7 magnitude bits moved to
+// f16 bits 7..13 read as an f16 equal e4m3 * 2^-8 for normals and subnormals
+// alike.  PRMT + shift on the integer pipe keeps the conversion pipe free.
+template <int J>
+__device__ __forceinline__ uint32_t scale_pair_x2(uint32_t w) {
+  constexpr uint32_t sel = (J << 12) | (4 << 8) | (J << 4) | 4;  // bytes [0, sJ, 0, sJ]
+  uint32_t r;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(w), "n"(sel));
+  return r >> 1;
+}
+
+// Scale bytes 0 and 1 of the low half of `w` as f16x2 (s0 -> low, s1 -> high), times 2^-8.
+__device__ __forceinline__ uint32_t scale_lohi_x2(uint32_t w) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(w), "n"(0x1404));  // bytes [0, s0, 0, s1]
+  return r >> 1;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// f32 += f16 * f16 (mixed-precision fma; the products of an E2M1 value and an
+// 8-significant-bit activation are exact in f32).
+__device__ __forceinline__ float fma_f16lo(uint32_t a2, uint32_t b2, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, %3;\n\t}"
+      : "=f"(d)
+      : "r"(a2), "r"(b2), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_f16hi(uint32_t a2, uint32_t b2, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, ah, bh, %3;\n\t}"
+      : "=f"(d)
+      : "r"(a2), "r"(b2), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ float f16lo_to_f32(uint32_t h2) {
+  float f;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(h2));
+  return f;
+}
+__device__ __forceinline__ float f16hi_to_f32(uint32_t h2) {
+  float f;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(h2));
+  return f;
+}
+
+// D += A * B, m16n8k16, f16 operands, f32 accumulate.
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(const void* p) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_addr(p)));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)));
+  return v;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+// float -> bf16 bits, round to nearest even (finite inputs).
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+  return r;
+}
+
+// float -> f16 bits, round to nearest even.
+__device__ __forceinline__ uint16_t f32_to_f16_bits(float f) {
+  uint16_t r;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(f));
+  return r;
+}
+
+// Power-of-two activation rescale: the exponent s with amax * 2^s in [2^14, 2^15),
+// so every bf16 value of the row lands in f16's normal range, or is still exact
+// in f16's subnormal range down to 2^-31 of the row maximum.  0 for an all-zero
+// row; clamped to [-100, 100] so 2^s and the epilogue's 2^(8-s) stay normal fp32.
+__device__ __forceinline__ int pow2_rescale_exponent(float amax) {
+  if (!(amax > 0.f)) return 0;
+  const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF);  // biased exponent
+  const int s = 141 - e;  // amax in [2^(e-127), 2^(e-126)) -> times 2^(141-e) in [2^14, 2^15)
+  return s > 100 ? 100 : (s < -100 ? -100 : s);
+}
+
+__device__ __forceinline__ float exp2i(int e) {
+  // 2^e for e in [-126, 127]; callers keep e in range.
+  return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,180 @@
+// Offline NVFP4 quantizer and repack kernels.
+//
+// Quantizer: formula (1) of nvfp4_skinny.h in reverse (E2M1 weights, E4M3
+// group-16 scales, fp32 global scale -- gemma-cuda-hybrid README, "Everything
+// it has / Inference engine").  Every quotient is an IEEE fp32 operation and
+// the code decisions use the hardware round-to-nearest-even saturating
+// converters, so the codes are a function of fp32 values only.
+//
+// Repack: canonical bytes -> the tiled layout documented in nvfp4_skinny.h
+// ("offline weight repack into mma-fragment order" -- gemma-cuda-hybrid README,
+// "NVFP4-specific").
+#pragma once
+
+#include "common.cuh"
+
+namespace nvfp4 {
+
+// Per-matrix amax of |w| as the bit pattern of a non-negative float: for such
+// floats unsigned integer order equals numeric order, so atomicMax is exact and
+// order-independent.
+__global__ void quant_amax_kernel(const float* __restrict__ w, size_t per_matrix, unsigned* __restrict__ amax_bits) {
+  const int e = blockIdx.y;
+  const float* src = w + static_cast<size_t>(e) * per_matrix;
+  unsigned best = 0;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < per_matrix;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const unsigned b = __float_as_uint(fabsf(src[i]));
+    best = b > best ? b : best;
+  }
+  for (int off = 16; off > 0; off >>= 1) {
+    const unsigned o = __shfl_xor_sync(0xffffffffu, best, off);
+    best = o > best ? o : best;
+  }
+  __shared__ unsigned warp_best[32];
+  if ((threadIdx.x & 31) == 0) warp_best[threadIdx.x >> 5] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned b = 0;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) b = warp_best[i] > b ? warp_best[i] : b;
+    atomicMax(&amax_bits[e], b);
+  }
+}
+
+__device__ __forceinline__ uint32_t e4m3_code_rne(float t) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(t));  // t -> low byte
+  return r & 0xFF;
+}
+
+// (hi, lo) -> one byte of two E2M1 codes: lo in the low nibble.
+__device__ __forceinline__ uint32_t e2m1x2_code_rne(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  // keep the sign of values that round to zero (-tiny -> code 8)
+  r &= 0x77u;
+  r |= (__float_as_uint(lo) >> 31) << 3;
+  r |= (__float_as_uint(hi) >> 31) << 7;
+  return r;
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  const uint32_t e = (c >> 3) & 0xF, m = c & 7;
+  const float mag = e == 0 ? static_cast<float>(m) * 0.001953125f  // m/8 * 2^-6
+                           : __uint_as_float(((e + 120u) << 23) | (m << 20));  // (1+m/8) * 2^(e-7)
+  return (c & 0x80) ? -mag : mag;
+}
+
+// One thread per 16-element group.
+__global__ void quant_groups_kernel(const float* __restrict__ w, int n, int k, const unsigned* __restrict__ amax_bits,
+                                    uint8_t* __restrict__ nibbles, uint8_t* __restrict__ scales,
+                                    float* __restrict__ global_scale) {
+  const int e = blockIdx.y;
+  const int groups_per_row = k / 16;
+  const size_t groups = static_cast<size_t>(n) * groups_per_row;
+  const float amax = __uint_as_float(amax_bits[e]);
+  const float g = __fdiv_rn(amax, 2688.0f);
+  if (blockIdx.x == 0 && threadIdx.x == 0) global_scale[e] = g;
+  for (size_t gi = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; gi < groups;
+       gi += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t base = (static_cast<size_t>(e) * n * k) + gi * 16;
+    const float4* src = reinterpret_cast<const float4*>(w + base);
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 f = src[i];
+      v[4 * i] = f.x, v[4 * i + 1] = f.y, v[4 * i + 2] = f.z, v[4 * i + 3] = f.w;
+    }
+    float bmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+    uint32_t s_code = 0;
+    float denom = 0.f;
+    if (g > 0.f) {
+      const float t = __fdiv_rn(__fdiv_rn(bmax, 6.0f), g);
+      s_code = e4m3_code_rne(t);
+      denom = __fmul_rn(e4m3_value(s_code), g);
+    }
+    uint32_t packed[2] = {0u, 0u};
+    if (denom > 0.f) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t b = e2m1x2_code_rne(__fdiv_rn(v[2 * i], denom), __fdiv_rn(v[2 * i + 1], denom));
+        packed[i >> 2] |= b << (8 * (i & 3));
+      }
+    }
+    uint2* dst = reinterpret_cast<uint2*>(nibbles + (static_cast<size_t>(e) * n * k) / 2 + gi * 8);
+    *dst = make_uint2(packed[0], packed[1]);
+    scales[static_cast<size_t>(e) * groups + gi] = static_cast<uint8_t>(s_code);
+  }
+}
+
+// One thread per 16-byte output chunk (36 chunks per 576-byte tile).
+__global__ void repack_kernel(const uint8_t* __restrict__ nib, const uint8_t* __restrict__ sc, int n, int k, int nb,
+                              int kc_count, bool gated, size_t tiles_total, uint8_t* __restrict__ out) {
+  const size_t chunks = tiles_total * 36;
+  const int kh = k / 2, kg = k / 16, inter = n / 2;
+  const size_t tiles_per_matrix = static_cast<size_t>(nb) * kc_count;
+  for (size_t c = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks;
+       c += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t tile = c / 36;
+    const int part = static_cast<int>(c % 36);
+    const int e = static_cast<int>(tile / tiles_per_matrix);
+    const size_t tm = tile % tiles_per_matrix;
+    const int rb = static_cast<int>(tm / kc_count), kc = static_cast<int>(tm % kc_count);
+    const uint8_t* nib_e = nib + static_cast<size_t>(e) * n * kh;
+    const uint8_t* sc_e = sc + static_cast<size_t>(e) * n * kg;
+    // source row of destination row `dr`, or -1 for padding
+    auto src_row = [&](int dr) -> int {
+      if (gated) {
+        const int blk = dr >> 4, j = dr & 15;
+        return (j < 8) ? (8 * blk + j) : (inter + 8 * blk + (j - 8));
+      }
+      return dr < n ? dr : -1;
+    };
+    uint32_t words[4];
+    if (part < 32) {
+      const int g = part >> 2, t = part & 3;
+#pragma unroll
+      for (int kt = 0; kt < 4; ++kt) {
+        uint32_t wv = 0;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int dr = rb * 16 + g + 8 * (r & 1);
+          const int col = kc * 64 + kt * 16 + 2 * t + 8 * (r >> 1);
+          const int sr = src_row(dr);
+          uint32_t byte = 0;
+          if (sr >= 0 && col < k) {
+            byte = nib_e[static_cast<size_t>(sr) * kh + col / 2];
+            if (sc_e[static_cast<size_t>(sr) * kg + col / 16] & 0x80) byte ^= 0x88u;  // fold a negative scale
+          }
+          wv |= byte << (8 * r);
+        }
+        words[kt] = wv;
+      }
+    } else {
+      // scale bytes 16*(part-32) .. +15 of the 64-byte scale block: byte j -> g = j/8, kt = (j%8)/2, h = j%2
+#pragma unroll
+      for (int wi = 0; wi < 4; ++wi) {
+        uint32_t wv = 0;
+#pragma unroll
+        for (int bi = 0; bi < 4; ++bi) {
+          const int j = 16 * (part - 32) + 4 * wi + bi;
+          const int g = j >> 3, kt = (j & 7) >> 1, h = j & 1;
+          const int dr = rb * 16 + g + 8 * h;
+          const int grp = kc * 4 + kt;
+          const int sr = src_row(dr);
+          uint32_t byte = 0;
+          if (sr >= 0 && grp < kg) byte = sc_e[static_cast<size_t>(sr) * kg + grp] & 0x7Fu;
+          wv |= byte << (8 * bi);
+        }
+        words[wi] = wv;
+      }
+    }
+    reinterpret_cast<uint4*>(out)[c] = make_uint4(words[0], words[1], words[2], words[3]);
+  }
+}
+
+}  // namespace nvfp4

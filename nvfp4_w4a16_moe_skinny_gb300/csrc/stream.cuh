@@ -1,0 +1,214 @@
+// Per-warp weight streaming and the two tile consumers (sm_103a).
+//
+// Every warp owns a private ring of `ns` stages in shared memory.  Lane 0 fills
+// a stage with one 1-D bulk copy (TMA engine, L2 evict-first) of a contiguous
+// run of up to kTPS 576-byte tiles; the whole warp waits on the stage's
+// mbarrier; when the warp has consumed a stage, lane 0 refills it with the
+// chunk `ns` positions ahead.  No stage is shared between warps, so the only
+// synchronisation is the mbarrier (copy -> warp) and __syncwarp (warp -> refill).
+//
+// Tile consumers:
+//  * mma_tile<NT>: tensor cores (m16n8k16, f16 in, f32 accumulate); weights are
+//    the 16-row A operand and up to 8*NT tokens the N operand.  One 16-byte
+//    shared load per lane yields the A fragments of four 16-column groups; each
+//    E2M1 pair goes through the hardware converter and is multiplied in f16 by
+//    its E4M3 scale (exact: the product has at most 6 significant bits).
+//  * core_tile<MT>: CUDA cores for up to 7 tokens.  Lane (g, q) takes rows g and
+//    g+8 over 16-column group q of the tile; it sums E2M1 x activation products
+//    in f32 (mixed-precision FMA; the products are exact), scales each group
+//    sum once, and the cross-lane reduction is left to warp shuffles.
+#pragma once
+
+#include "common.cuh"
+
+namespace nvfp4 {
+
+constexpr int kTPS = 4;  // tiles per ring stage (2304 bytes)
+constexpr int kStageBytes = kTPS * kTileBytes;
+
+// x fragments for the MMA path, per 64-column chunk and 8-token group: 32 lanes x
+// 8 words (f16x2).  Lane (g, t), word 2*kt + h holds tokens slot g, columns
+// 16*kt + 2*t + 8*h (+1) of the chunk -- the m16n8k16 B fragment.
+constexpr int kXFragChunkBytes = 1024;
+// x for the CUDA-core path, per 64-column chunk and token: 32 f16x2 words (pairs).
+constexpr int kXCoreChunkBytes = 128;
+
+template <int NT>
+__device__ __forceinline__ void mma_step(uint32_t word, uint32_t sg, uint32_t sg8, const uint32_t (&b0)[NT],
+                                         const uint32_t (&b1)[NT], float (&acc)[NT][4]) {
+  uint32_t h[4];
+  e2m1x8_to_f16x2(word, h);
+  uint32_t a[4];
+  a[0] = hmul2(h[0], sg);   // row g,   columns 2t, 2t+1
+  a[1] = hmul2(h[1], sg8);  // row g+8, columns 2t, 2t+1
+  a[2] = hmul2(h[2], sg);   // row g,   columns 2t+8, 2t+9
+  a[3] = hmul2(h[3], sg8);  // row g+8, columns 2t+8, 2t+9
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) mma_f16(acc[nt], a, b0[nt], b1[nt]);
+}
+
+// One 16x64 tile against x fragments `xf` (NT * 1024 bytes for this chunk).
+// acc[nt] is the C fragment: [0],[1] = row g, tokens 8nt+2t, +1; [2],[3] = row g+8.
+template <int NT>
+__device__ __forceinline__ void mma_tile(const uint8_t* tile, const uint8_t* xf, int lane, float (&acc)[NT][4]) {
+  const uint4 wv = lds128(tile + lane * 16);
+  const uint2 sv = lds64(tile + kTileNibBytes + (lane >> 2) * 8);
+  uint4 xa[NT], xb[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    xa[nt] = lds128(xf + nt * kXFragChunkBytes + lane * 32);
+    xb[nt] = lds128(xf + nt * kXFragChunkBytes + lane * 32 + 16);
+  }
+  uint32_t b0[NT], b1[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) b0[nt] = xa[nt].x, b1[nt] = xa[nt].y;
+  mma_step<NT>(wv.x, scale_pair_x2<0>(sv.x), scale_pair_x2<1>(sv.x), b0, b1, acc);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) b0[nt] = xa[nt].z, b1[nt] = xa[nt].w;
+  mma_step<NT>(wv.y, scale_pair_x2<2>(sv.x), scale_pair_x2<3>(sv.x), b0, b1, acc);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) b0[nt] = xb[nt].x, b1[nt] = xb[nt].y;
+  mma_step<NT>(wv.z, scale_pair_x2<0>(sv.y), scale_pair_x2<1>(sv.y), b0, b1, acc);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) b0[nt] = xb[nt].z, b1[nt] = xb[nt].w;
+  mma_step<NT>(wv.w, scale_pair_x2<2>(sv.y), scale_pair_x2<3>(sv.y), b0, b1, acc);
+}
+
+__device__ __forceinline__ uint32_t lds_u16(const void* p) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(smem_addr(p)));
+  return v;
+}
+
+// One 16x64 tile on CUDA cores.  xw: the chunk's x words [MT][32] (pair pp =
+// columns 2pp, 2pp+1).  acc[m][0] = row g, acc[m][1] = row g+8 (partial over
+// this lane's group q; summed over q by the caller).
+template <int MT>
+__device__ __forceinline__ void core_tile(const uint8_t* tile, const uint8_t* xw, int g, int q, float (&acc)[MT][2]) {
+  const uint32_t sp = scale_lohi_x2(lds_u16(tile + kTileNibBytes + 8 * g + 2 * q));
+  const float sg = f16lo_to_f32(sp), sg8 = f16hi_to_f32(sp);  // scale * 2^-8
+  const int h = g >> 1;
+  float pa[MT], pb[MT], pc[MT], pd[MT];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) pa[m] = pb[m] = pc[m] = pd[m] = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    // rotate the 4 lane-chunks by g/2 so the 32 lanes hit 32 distinct banks
+    const int t = (j + h) & 3;
+    const uint32_t word = lds32(tile + 16 * (4 * g + t) + 4 * q);
+    uint32_t hh[4];
+    e2m1x8_to_f16x2(word, hh);
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      const uint32_t x0 = lds32(xw + m * kXCoreChunkBytes + (8 * q + t) * 4);
+      const uint32_t x1 = lds32(xw + m * kXCoreChunkBytes + (8 * q + t + 4) * 4);
+      pa[m] = fma_f16lo(hh[0], x0, pa[m]);
+      pb[m] = fma_f16hi(hh[0], x0, pb[m]);
+      pa[m] = fma_f16lo(hh[2], x1, pa[m]);
+      pb[m] = fma_f16hi(hh[2], x1, pb[m]);
+      pc[m] = fma_f16lo(hh[1], x0, pc[m]);
+      pd[m] = fma_f16hi(hh[1], x0, pd[m]);
+      pc[m] = fma_f16lo(hh[3], x1, pc[m]);
+      pd[m] = fma_f16hi(hh[3], x1, pd[m]);
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    acc[m][0] = fmaf(pa[m] + pb[m], sg, acc[m][0]);
+    acc[m][1] = fmaf(pc[m] + pd[m], sg8, acc[m][1]);
+  }
+}
+
+// Shared-memory ring of one warp.
+struct Ring {
+  uint8_t* buf;    // ns * kStageBytes
+  uint64_t* bar;   // ns mbarriers
+  int ns;
+};
+
+__device__ __forceinline__ void ring_init(const Ring& r, int lane) {
+  if (lane == 0) {
+    for (int s = 0; s < r.ns; ++s) mbar_init(&r.bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+}
+
+// Lane 0 only: copy `ntiles` tiles from `src` into stage s.
+__device__ __forceinline__ void ring_issue(const Ring& r, int s, const uint8_t* src, int ntiles, uint64_t policy) {
+  const uint32_t bytes = static_cast<uint32_t>(ntiles * kTileBytes);
+  mbar_arrive_expect_tx(&r.bar[s], bytes);
+  bulk_g2s(r.buf + s * kStageBytes, src, bytes, &r.bar[s], policy);
+}
+
+// Stage the bf16 activations of `rows` token slots over columns [col0, col0 +
+// 64*nchunks) into shared memory as f16, each token rescaled by 2^sigma[slot].
+// tok_row(slot) gives the source row of x (or -1 for an empty slot); k = row length.
+// MMA layout (fragments) or CUDA-core layout (pairs), see the constants above.
+template <bool kMMA, int SLOTS, typename TokRow>
+__device__ __forceinline__ void stage_x(const uint16_t* __restrict__ x, int k, int col0, int nchunks, TokRow tok_row,
+                                        const int* sigma, uint8_t* xs) {
+  uint32_t* xw = reinterpret_cast<uint32_t*>(xs);
+  if constexpr (kMMA) {
+    constexpr int NT = (SLOTS + 7) / 8;
+    const int words = nchunks * NT * 256;
+    for (int i = threadIdx.x; i < words; i += blockDim.x) {
+      const int kcl = i / (NT * 256);
+      const int rem = i - kcl * NT * 256;
+      const int nt = rem >> 8, ln = (rem >> 3) & 31, wd = rem & 7;
+      const int g = ln >> 2, t = ln & 3, kt = wd >> 1, hf = wd & 1;
+      const int slot = nt * 8 + g;
+      const int col = col0 + kcl * 64 + kt * 16 + 2 * t + 8 * hf;
+      uint32_t v = 0;
+      const int row = slot < SLOTS ? tok_row(slot) : -1;
+      if (row >= 0 && col < k) {
+        const uint32_t pair = __ldg(reinterpret_cast<const uint32_t*>(x + static_cast<size_t>(row) * k + col));
+        const float sc = exp2i(sigma[slot]);
+        const float lo = __uint_as_float(pair << 16) * sc, hi = __uint_as_float(pair & 0xFFFF0000u) * sc;
+        v = static_cast<uint32_t>(f32_to_f16_bits(lo)) | (static_cast<uint32_t>(f32_to_f16_bits(hi)) << 16);
+      }
+      xw[i] = v;
+    }
+  } else {
+    const int words = nchunks * SLOTS * 32;
+    for (int i = threadIdx.x; i < words; i += blockDim.x) {
+      const int kcl = i / (SLOTS * 32);
+      const int rem = i - kcl * SLOTS * 32;
+      const int slot = rem >> 5, pp = rem & 31;
+      const int col = col0 + kcl * 64 + 2 * pp;
+      uint32_t v = 0;
+      const int row = tok_row(slot);
+      if (row >= 0 && col < k) {
+        const uint32_t pair = __ldg(reinterpret_cast<const uint32_t*>(x + static_cast<size_t>(row) * k + col));
+        const float sc = exp2i(sigma[slot]);
+        const float lo = __uint_as_float(pair << 16) * sc, hi = __uint_as_float(pair & 0xFFFF0000u) * sc;
+        v = static_cast<uint32_t>(f32_to_f16_bits(lo)) | (static_cast<uint32_t>(f32_to_f16_bits(hi)) << 16);
+      }
+      xw[i] = v;
+    }
+  }
+}
+
+// Per-slot power-of-two exponents from the amax of each token row over
+// columns [c0, c1): one warp per slot (slots <= warps per CTA).  Writes sigma[slot].
+template <typename TokRow>
+__device__ __forceinline__ void token_sigma(const uint16_t* __restrict__ x, int k, int c0, int c1, int slots,
+                                            TokRow tok_row, int* sigma) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int slot = warp; slot < slots; slot += blockDim.x >> 5) {
+    const int row = tok_row(slot);
+    float am = 0.f;
+    if (row >= 0) {
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(x + static_cast<size_t>(row) * k);
+      for (int c = c0 + 2 * lane; c < c1; c += 64) {
+        const uint32_t pair = __ldg(src + c / 2);
+        am = fmaxf(am, fmaxf(fabsf(__uint_as_float(pair << 16)), fabsf(__uint_as_float(pair & 0xFFFF0000u))));
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
+    if (lane == 0) sigma[slot] = pow2_rescale_exponent(am);
+  }
+}
+
+}  // namespace nvfp4

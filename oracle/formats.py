@@ -115,10 +115,12 @@ def global_scale(w: np.ndarray) -> np.float32:
     return np.float32(amax / np.float32(E4M3_MAX * E2M1_MAX))
 
 
-def quantize_matrix(w: np.ndarray):
+def quantize_matrix(w: np.ndarray, chunk_rows: int = 4096):
     """Quantize one fp32 matrix [N, K] (K % 16 == 0) to canonical NVFP4.
 
-    Returns (nibbles uint8 [N, K/2], scales uint8 [N, K/16], g float32).
+    Returns (nibbles uint8 [N, K/2], scales uint8 [N, K/16], g float32).  Rows are
+    processed in chunks only to bound host memory; every row is independent once
+    g is known.
     """
     w = np.ascontiguousarray(w, dtype=np.float32)
     n, k = w.shape
@@ -127,6 +129,16 @@ def quantize_matrix(w: np.ndarray):
     g = global_scale(w)
     if g == 0:
         return (np.zeros((n, k // 2), np.uint8), np.zeros((n, k // 16), np.uint8), np.float32(0))
+    nib = np.empty((n, k // 2), np.uint8)
+    sc = np.empty((n, k // 16), np.uint8)
+    for lo in range(0, n, chunk_rows):
+        hi = min(n, lo + chunk_rows)
+        nib[lo:hi], sc[lo:hi] = _quantize_rows(w[lo:hi], g)
+    return nib, sc, g
+
+
+def _quantize_rows(w: np.ndarray, g: np.float32):
+    n, k = w.shape
     blocks = w.reshape(n, k // 16, 16)
     bmax = np.max(np.abs(blocks), axis=2).astype(np.float32)
     t = (bmax / np.float32(E2M1_MAX)).astype(np.float32) / g          # two fp32 divisions
@@ -138,7 +150,7 @@ def quantize_matrix(w: np.ndarray):
     q = e2m1_encode(v)
     q = np.where((s_val == 0)[:, :, None], np.uint8(0), q).reshape(n, k)
     nib = (q[:, 0::2] & 0xF) | ((q[:, 1::2] & 0xF) << 4)
-    return nib.astype(np.uint8), s_code.reshape(n, k // 16), g
+    return nib.astype(np.uint8), s_code.reshape(n, k // 16)
 
 
 def quantize_stack(w: np.ndarray):

@@ -1,0 +1,225 @@
+"""GPU parity: quantizer, repack, dense skinny GEMM and lm_head argmax vs the FP64 oracle.
+
+All compute runs through the C ABI (libnvfp4skinny.so); the oracle runs on the host.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as F
+from oracle import gemm as OG
+from oracle import layout as OL
+from oracle import lm_head as OLM
+from nvfp4_w4a16_moe_skinny_gb300 import workloads as W
+from tests.gpu_helpers import bf16_to_f64, check_bound, dev, upload_bf16, upload_f32
+
+pytestmark = pytest.mark.gpu
+
+
+# ------------------------------------------------------------------ quantizer
+
+@pytest.mark.parametrize("n,k,seed", [(512, 256, 0), (40, 80, 1), (33, 16, 2), (16, 1024, 3)])
+def test_quantizer_bit_exact(lib, n, k, seed):
+    w = W.weight((n, k), seed) if seed else W.DenseCase.tiny().w()
+    nib, sc, g = lib.quantize(upload_f32(w))
+    onib, osc, og = F.quantize_matrix(w)
+    assert g.item() == float(og)
+    assert np.array_equal(sc.cpu().numpy(), osc)
+    assert np.array_equal(nib.cpu().numpy(), onib)
+
+
+def test_quantizer_special_values(lib):
+    """Zero and underflowing blocks, sign of zero, and exact E2M1 ties: with amax =
+    2688 * 2^-10 the global scale is exactly 2^-10 and a block whose maximum is
+    6 * 2^-10 gets scale 1, so w / (scale * g) hits the rounding midpoints exactly."""
+    rng = np.random.default_rng(21)
+    w = (rng.standard_normal((32, 64)) * 0.1).astype(np.float32)
+    w[2, 0] = 2688.0 * 2.0 ** -10                    # global max -> g = 2^-10
+    w[0, :16] = 0.0                                  # zero block
+    w[1, 16:32] = 1e-12                              # block below the scale range
+    w[3, :] = -w[3, :]
+    w[4, 5] = -1e-9                                  # -tiny next to large values: code 8
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0], np.float32)
+    w[5, :16] = np.concatenate([ties, -ties]) * np.float32(2.0 ** -10)
+    nib, sc, g = lib.quantize(upload_f32(w))
+    onib, osc, og = F.quantize_matrix(w)
+    assert g.item() == float(og)
+    assert np.array_equal(sc.cpu().numpy(), osc)
+    assert np.array_equal(nib.cpu().numpy(), onib)
+    z_nib, z_sc, z_g = lib.quantize(torch.zeros((16, 32), device=dev()))
+    assert z_g.item() == 0.0 and not z_nib.any().item() and not z_sc.any().item()
+
+
+def test_quantizer_stacked(lib):
+    w = np.stack([W.weight((32, 128), 100 + e) * (e + 1) for e in range(3)])
+    nib, sc, g = lib.quantize(upload_f32(w))
+    for e in range(3):
+        onib, osc, og = F.quantize_matrix(w[e])
+        assert g[e].item() == float(og)
+        assert np.array_equal(sc[e].cpu().numpy(), osc)
+        assert np.array_equal(nib[e].cpu().numpy(), onib)
+
+
+# ------------------------------------------------------------------ repack
+
+@pytest.mark.parametrize("e,n,k,gated", [(1, 16, 64, False), (2, 40, 80, False), (1, 1000, 320, False),
+                                         (3, 32, 128, True), (2, 48, 16, True)])
+def test_repack_bytes_bit_exact(lib, e, n, k, gated):
+    rng = np.random.default_rng(n * 7 + k)
+    nib = rng.integers(0, 256, (e, n, k // 2), dtype=np.uint8)
+    sc = rng.integers(0, 127, (e, n, k // 16), dtype=np.uint8)
+    wt = lib.repack(torch.from_numpy(nib).to(dev()), torch.from_numpy(sc).to(dev()),
+                    torch.ones(e, device=dev()), gated=gated)
+    assert wt.data.numel() == OL.repacked_bytes(n, k, e)
+    assert np.array_equal(wt.data.cpu().numpy(), OL.repack(nib, sc, gated))
+
+
+def test_repack_folds_negative_scales(lib):
+    rng = np.random.default_rng(5)
+    n, k = 32, 64
+    nib = rng.integers(0, 256, (n, k // 2), dtype=np.uint8)
+    sc = rng.integers(1, 127, (n, k // 16), dtype=np.uint8)
+    sc[::3, 1] |= 0x80                                   # some negative scales
+    wt = lib.repack(torch.from_numpy(nib).to(dev()), torch.from_numpy(sc).to(dev()), torch.ones(1, device=dev()))
+    nib2, sc2 = OL.unrepack(wt.data.cpu().numpy(), n, k)
+    assert not (sc2 & 0x80).any()
+    assert np.array_equal(F.dequantize_matrix(nib2[0], sc2[0], 1.0), F.dequantize_matrix(nib, sc, 1.0))
+
+
+# ------------------------------------------------------------------ dense GEMM
+
+def _dense(lib, m, n, k, w_seed, x_seed):
+    w = W.weight((n, k), w_seed)
+    xb, _ = W.activations((m, k), x_seed)
+    wt = lib.prepare(upload_f32(w))
+    y = lib.gemm(wt, upload_bf16(xb))
+    torch.cuda.synchronize()
+    nib, sc, g = F.quantize_matrix(w)
+    exact, _, absy = OG.nvfp4_gemm(nib, sc, g, W.bf16_bits_to_f32(xb).astype(np.float64))
+    return bf16_to_f64(y), exact, absy
+
+
+def test_tiny_gemm_config0(lib):
+    case = W.DenseCase.tiny()
+    w = case.w()
+    xb, xf = case.x()
+    wt = lib.prepare(upload_f32(w))
+    y = lib.gemm(wt, upload_bf16(xb))
+    torch.cuda.synchronize()
+    nib, sc, g = F.quantize_matrix(w)
+    exact, _, absy = OG.nvfp4_gemm(nib, sc, g, xf.astype(np.float64))
+    check_bound(bf16_to_f64(y), exact, absy, True, "tiny gemm")
+    assert lib.device_error() == 0
+
+
+@pytest.mark.parametrize("m", list(range(1, 17)))
+@pytest.mark.parametrize("n,k", [(40, 80), (1000, 320), (272, 1088)])
+def test_gemm_ragged_all_m(lib, m, n, k):
+    got, exact, absy = _dense(lib, m, n, k, 1000 + n + k, 2000 + m)
+    check_bound(got, exact, absy, True, f"gemm m={m} n={n} k={k}")
+
+
+@pytest.mark.parametrize("m", [1, 4, 15, 16])
+@pytest.mark.parametrize("n", [4096, 14336])
+def test_gemm_config1_full_size(lib, m, n):
+    case = W.DenseCase.sweep(m, n)
+    w = case.w()
+    xb, xf = case.x()
+    wt = lib.prepare(upload_f32(w))
+    y = lib.gemm(wt, upload_bf16(xb))
+    torch.cuda.synchronize()
+    nib, sc, g = F.quantize_matrix(w)
+    exact, _, absy = OG.nvfp4_gemm(nib, sc, g, xf.astype(np.float64))
+    check_bound(bf16_to_f64(y), exact, absy, True, f"config1 m={m} n={n}")
+    assert lib.device_error() == 0
+
+
+def test_gemm_repeat_calls_stable(lib):
+    """Back-to-back calls on one workspace (split-K counters stay consistent)."""
+    case = W.DenseCase.sweep(16, 4096)
+    w = case.w()
+    xb, _ = case.x()
+    wt = lib.prepare(upload_f32(w))
+    x = upload_bf16(xb)
+    first = lib.gemm(wt, x).clone()
+    for _ in range(5):
+        again = lib.gemm(wt, x)
+        assert torch.equal(again, first)
+
+
+# ------------------------------------------------------------------ lm_head
+
+def _lm(lib, m, vocab, k, w_seed, x_seed, plant=None):
+    w = W.weight((vocab, k), w_seed)
+    xb, xf = W.activations((m, k), x_seed)
+    if plant is not None:
+        row, tok = plant
+        w[row] = np.sign(xf[tok]).astype(np.float32) * 0.05
+    wt = lib.prepare(upload_f32(w))
+    mx, idx = lib.lm_head_argmax(wt, upload_bf16(xb))
+    torch.cuda.synchronize()
+    nib, sc, g = F.quantize_matrix(w)
+    ref = OLM.lm_head_argmax(nib, sc, g, xf.astype(np.float64))
+    return mx.cpu().numpy(), idx.cpu().numpy(), ref, (nib, sc, g, xf)
+
+
+def _check_argmax(mx, idx, ref, parts, what):
+    nib, sc, g, xf = parts
+    for t in range(len(idx)):
+        lg, la = OLM.logits_rows(nib, sc, g, xf[t:t + 1].astype(np.float64), [idx[t], ref["argmax"][t]])
+        tol = 1e-3 * max(la[0, 0], la[0, 1])
+        gap = ref["max"][t] - ref["second"][t]
+        if gap > 2 * tol:
+            assert idx[t] == ref["argmax"][t], f"{what}: token {t} argmax {idx[t]} != {ref['argmax'][t]}"
+        else:   # a near-tie: the returned row must be a valid maximiser within the bound
+            assert ref["max"][t] - lg[0, 0] <= 2 * tol, f"{what}: token {t} near-tie row not maximal"
+        assert abs(mx[t] - lg[0, 0]) <= tol, f"{what}: token {t} max logit {mx[t]} vs {lg[0, 0]}"
+
+
+@pytest.mark.parametrize("m", [1, 3, 7, 8, 15, 16])
+@pytest.mark.parametrize("vocab,k", [(3000, 256), (1037, 2816)])
+def test_lm_head_small(lib, m, vocab, k):
+    mx, idx, ref, parts = _lm(lib, m, vocab, k, 300 + vocab, 400 + m)
+    _check_argmax(mx, idx, ref, parts, f"lm_head m={m} vocab={vocab}")
+
+
+def test_lm_head_planted_max_and_tie(lib):
+    m, vocab, k = 4, 2048, 256
+    w = W.weight((vocab, k), 77)
+    xb, xf = W.activations((m, k), 78)
+    w[1500] = np.sign(xf[2]).astype(np.float32) * 0.05   # token 2: planted winner
+    w[700] = w[1500]                                     # identical row, lower index: must win the tie
+    wt = lib.prepare(upload_f32(w))
+    mx, idx = lib.lm_head_argmax(wt, upload_bf16(xb))
+    torch.cuda.synchronize()
+    assert idx[2].item() == 700
+    nib, sc, g = F.quantize_matrix(w)
+    ref = OLM.lm_head_argmax(nib, sc, g, xf.astype(np.float64))
+    assert ref["argmax"][2] == 700
+    assert np.array_equal(idx.cpu().numpy(), ref["argmax"])
+
+
+@pytest.fixture(scope="module")
+def lm_head_full(lib):
+    """The full 262,144 x 2,816 lm_head: GPU-quantized for the kernel, oracle-quantized
+    on the host for the reference (the two quantizers are compared bit for bit on
+    sampled rows here and exhaustively on smaller shapes above)."""
+    case = W.LMHeadCase(m=1)
+    w = case.w_rows(0, case.vocab)
+    wt = lib.prepare(upload_f32(w))
+    nib, sc, g = F.quantize_matrix(w)
+    torch.cuda.synchronize()
+    return wt, nib, sc, g
+
+
+@pytest.mark.parametrize("m", [1, 15])
+def test_lm_head_config3_full_size(lib, lm_head_full, m):
+    wt, nib, sc, g = lm_head_full
+    assert wt.global_scale.item() == float(g)
+    xb, xf = W.LMHeadCase(m=m).x()
+    mx, idx = lib.lm_head_argmax(wt, upload_bf16(xb))
+    torch.cuda.synchronize()
+    ref = OLM.lm_head_argmax(nib, sc, g, xf.astype(np.float64), chunk_rows=16384)
+    _check_argmax(mx.cpu().numpy(), idx.cpu().numpy(), ref, (nib, sc, g, xf), f"lm_head full m={m}")
+    assert lib.device_error() == 0
