@@ -227,6 +227,66 @@ class Library:
             ctypes.byref(cd), sg, sd, out.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
         return out
 
+    # -------------------------------------------------------------- call plans
+    # Zero-argument callables with every ctypes argument built once, for timed
+    # loops where per-call Python marshalling would otherwise show up.
+    def plan_gemm(self, w: Weight, x: torch.Tensor, y: torch.Tensor, stream=None):
+        m = x.shape[0]
+        ws = self.workspace("gemm", self.lib.nvfp4_gemm_workspace_bytes(m, w.n, w.k), x.device)
+        cw = w.c()
+        args = (ctypes.byref(cw), x.data_ptr(), m, y.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream))
+        fn = self.lib.nvfp4_gemm
+
+        def run():
+            st = fn(*args)
+            if st:
+                raise NVFP4Error("nvfp4_gemm", st)
+        run.keep = (cw, ws)
+        return run
+
+    def plan_lm_head(self, w: Weight, x: torch.Tensor, max_logit: torch.Tensor, argmax: torch.Tensor, stream=None):
+        m = x.shape[0]
+        ws = self.workspace("lm_head", self.lib.lm_head_workspace_bytes(m, w.n), x.device)
+        cw = w.c()
+        args = (ctypes.byref(cw), x.data_ptr(), m, max_logit.data_ptr(), argmax.data_ptr(), ws.data_ptr(),
+                ws.numel(), _stream(stream))
+        fn = self.lib.lm_head_argmax
+
+        def run():
+            st = fn(*args)
+            if st:
+                raise NVFP4Error("lm_head_argmax", st)
+        run.keep = (cw, ws)
+        return run
+
+    def plan_moe(self, x, logits, top_k, gate_up: Weight, down: Weight, shared_gate_up: Weight, shared_down: Weight,
+                 route_out, out, stream=None):
+        """Router + grouped FFN as one callable (two C calls)."""
+        m, d = x.shape
+        e = logits.shape[1]
+        ids, probs, offsets, pairs = route_out
+        ws = self.workspace("moe", self.lib.moe_ffn_workspace_bytes(m, top_k, d, down.k), x.device)
+        cg, cd = gate_up.c(), down.c()
+        sg = shared_gate_up.c() if shared_gate_up is not None else None
+        sd = shared_down.c() if shared_down is not None else None
+        s = _stream(stream)
+        rargs = (logits.data_ptr(), m, e, top_k, ids.data_ptr(), probs.data_ptr(), offsets.data_ptr(),
+                 pairs.data_ptr(), s)
+        fargs = (x.data_ptr(), m, top_k, probs.data_ptr(), offsets.data_ptr(), pairs.data_ptr(), ctypes.byref(cg),
+                 ctypes.byref(cd), ctypes.byref(sg) if sg is not None else None,
+                 ctypes.byref(sd) if sd is not None else None, out.data_ptr(), ws.data_ptr(), ws.numel(), s)
+        route, ffn = self.lib.moe_route_topk, self.lib.moe_ffn_grouped
+
+        def run():
+            st = route(*rargs)
+            if st:
+                raise NVFP4Error("moe_route_topk", st)
+            st = ffn(*fargs)
+            if st:
+                raise NVFP4Error("moe_ffn_grouped", st)
+        run.keep = (cg, cd, sg, sd, ws)
+        return run
+
 
 _LIB = None
 

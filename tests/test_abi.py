@@ -1,0 +1,122 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every function the
+header declares, and its host-side size queries and argument checks behave as documented
+(each rejected call returns before any CUDA call)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from nvfp4_w4a16_moe_skinny_gb300 import build as B
+from oracle import layout as OL
+
+HEADER = os.path.join(B.INCLUDE, "nvfp4_skinny.h")
+
+
+@pytest.fixture(scope="module")
+def so():
+    B.build()
+    from nvfp4_w4a16_moe_skinny_gb300 import binding
+    lib = ctypes.CDLL(B.LIB)
+    binding._sig(lib)
+    return lib
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "return")))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for n in ("nvfp4_gemm", "moe_route_topk", "moe_ffn_grouped", "lm_head_argmax", "nvfp4_repack", "nvfp4_quantize"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(so):
+    missing = [n for n in declared_functions() if not hasattr(so, n)]
+    assert not missing, missing
+    from nvfp4_w4a16_moe_skinny_gb300 import binding
+    assert set(binding.EXPORTS) == set(declared_functions())
+
+
+def test_status_strings_and_version(so):
+    assert so.nvfp4_layout_version() == 1
+    for code, text in [(0, b"ok"), (1, b"null pointer"), (2, b"bad shape"), (4, b"workspace missing or too small")]:
+        assert so.nvfp4_status_string(code) == text
+
+
+@pytest.mark.parametrize("n,k,e", [(16, 64, 1), (40, 80, 2), (262144, 2816, 1), (1408, 2816, 128), (1, 16, 1)])
+def test_repacked_bytes_matches_layout_spec(so, n, k, e):
+    assert so.nvfp4_repacked_bytes(n, k, e) == OL.repacked_bytes(n, k, e)
+
+
+def test_sizes_reject_bad_shapes(so):
+    assert so.nvfp4_repacked_bytes(16, 24, 1) == 0          # k % 16
+    assert so.nvfp4_repacked_bytes(0, 64, 1) == 0
+    assert so.nvfp4_gemm_workspace_bytes(17, 64, 64) == 0   # m > 16
+    assert so.lm_head_workspace_bytes(0, 100) == 0
+    assert so.moe_ffn_workspace_bytes(15, 8, 2816, 704) == (15 * 8 + 15) * (704 * 2 + 2816 * 4)
+
+
+def _weight(data=1 << 20, gs=1 << 20, n=64, k=64, e=1, flags=0, version=1):
+    from nvfp4_w4a16_moe_skinny_gb300.binding import CWeight
+    return CWeight(data, gs, n, k, e, flags, version)
+
+
+def test_gemm_argument_errors_return_before_any_launch(so):
+    ws = ctypes.c_void_p(1 << 20)
+    x, y = ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 20)
+    assert so.nvfp4_gemm(None, x, 1, y, ws, 1 << 20, None) == 1
+    w = _weight(data=0)
+    assert so.nvfp4_gemm(ctypes.byref(w), x, 1, y, ws, 1 << 20, None) == 1
+    w = _weight(version=2)
+    assert so.nvfp4_gemm(ctypes.byref(w), x, 1, y, ws, 1 << 20, None) == 5
+    w = _weight(flags=1)
+    assert so.nvfp4_gemm(ctypes.byref(w), x, 1, y, ws, 1 << 20, None) == 5
+    w = _weight(k=72)
+    assert so.nvfp4_gemm(ctypes.byref(w), x, 1, y, ws, 1 << 20, None) == 2
+    w = _weight()
+    assert so.nvfp4_gemm(ctypes.byref(w), x, 0, y, ws, 1 << 20, None) == 2
+    assert so.nvfp4_gemm(ctypes.byref(w), x, 17, y, ws, 1 << 20, None) == 2
+    assert so.nvfp4_gemm(ctypes.byref(w), ctypes.c_void_p((1 << 20) + 8), 1, y, ws, 1 << 20, None) == 3
+    assert so.nvfp4_gemm(ctypes.byref(w), x, 1, y, ws, 16, None) == 4
+    assert so.nvfp4_gemm(ctypes.byref(w), x, 1, y, None, 1 << 20, None) == 4
+    w = _weight(data=(1 << 20) + 4)
+    assert so.nvfp4_gemm(ctypes.byref(w), x, 1, y, ws, 1 << 20, None) == 3
+
+
+def test_lm_head_and_moe_argument_errors(so):
+    p = ctypes.c_void_p(1 << 20)
+    w = _weight()
+    assert so.lm_head_argmax(ctypes.byref(w), p, 1, None, p, p, 1 << 20, None) == 1
+    assert so.lm_head_argmax(ctypes.byref(w), p, 17, p, p, p, 1 << 20, None) == 2
+    assert so.lm_head_argmax(ctypes.byref(w), p, 1, p, p, p, 8, None) == 4
+    assert so.moe_route_topk(p, 15, 128, 0, p, p, p, p, None) == 2           # top_k < 1
+    assert so.moe_route_topk(p, 15, 4, 8, p, p, p, p, None) == 2             # top_k > n_experts
+    assert so.moe_route_topk(p, 15, 2048, 8, p, p, p, p, None) == 2          # n_experts > 1024
+    assert so.moe_route_topk(None, 15, 128, 8, p, p, p, p, None) == 1
+    gu = _weight(n=1408, k=2816, e=128, flags=1)
+    dn = _weight(n=2816, k=704, e=128)
+    args = [p, 15, 8, p, p, p, ctypes.byref(gu), ctypes.byref(dn), None, None, p, p, 1 << 30, None]
+    bad = list(args)
+    bad[7] = ctypes.byref(_weight(n=2816, k=704, e=64))                    # expert count mismatch
+    assert so.moe_ffn_grouped(*bad) == 2
+    bad = list(args)
+    bad[6] = ctypes.byref(_weight(n=1408, k=2816, e=128, flags=0))         # gate_up must be gated
+    assert so.moe_ffn_grouped(*bad) == 5
+    bad = list(args)
+    bad[8] = ctypes.byref(_weight(n=1408, k=2816, flags=1))                # shared gate_up without down
+    assert so.moe_ffn_grouped(*bad) == 1
+    bad = list(args)
+    bad[12] = 1024                                                          # workspace too small
+    assert so.moe_ffn_grouped(*bad) == 4
+
+
+def test_binding_refuses_to_run_without_the_library(tmp_path):
+    from nvfp4_w4a16_moe_skinny_gb300 import binding
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        binding.Library(str(tmp_path / "missing.so"))
