@@ -111,10 +111,9 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_kernel(const SkinnyParams 
   // activations of this CTA's k-slice -> shared memory (f16, per-token 2^sigma)
   const int col_lo = kc0 * kTileK, col_hi = min(kc1 * kTileK, p.k);
   auto tok_row = [&](int slot) -> int { return slot < p.m ? slot : -1; };
-  token_sigma(p.x, p.k, col_lo, col_hi, SLOTS, tok_row, sigma);
-  __syncthreads();
+  (void)col_hi;
+  stage_tokens<kMMA, SLOTS>(p.x, p.k, col_lo, kcs, tok_row, reinterpret_cast<unsigned*>(red_v), sigma, xs);
   if (threadIdx.x < SLOTS) mul[threadIdx.x] = __ldg(p.gscale) * exp2i(8 - sigma[threadIdx.x]);
-  stage_x<kMMA, SLOTS>(p.x, p.k, col_lo, kcs, tok_row, sigma, xs);
   __syncthreads();
 
   const int g = lane >> 2, t4 = lane & 3;

@@ -144,7 +144,7 @@ __host__ __device__ inline size_t moe_smem_bytes(bool mma, int slots, int kc, in
   const size_t ring = static_cast<size_t>(kWarps) * ns * kStageBytes;
   const size_t bars = static_cast<size_t>(kWarps) * ns * 8;
   const size_t xs = mma ? static_cast<size_t>(nt) * kc * kXFragChunkBytes : static_cast<size_t>(slots) * kc * kXCoreChunkBytes;
-  const size_t misc = 16 * 4 * 4 + (static_cast<size_t>(n_experts) + 2) * 4 + 16;
+  const size_t misc = 16 * 4 * 5 + (static_cast<size_t>(n_experts) + 2) * 4 + 16;
   return ring + bars + xs + misc;
 }
 
@@ -172,7 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_ffn_kernel(const MoEParams p)
   float* mul = reinterpret_cast<float*>(sigma + 16);
   int* slot_row = reinterpret_cast<int*>(mul + 16);   // activation row of each token slot
   int* slot_out = slot_row + 16;                      // output row (pair index) of each slot
-  int* seg_list = slot_out + 16;                      // [n_experts + 1]
+  unsigned* s_amax = reinterpret_cast<unsigned*>(slot_out + 16);
+  int* seg_list = reinterpret_cast<int*>(s_amax + 16);  // [n_experts + 1]
   int* n_seg_s = seg_list + p.n_experts + 1;
 
   // ---- active segments (warp 0, ballots in ascending expert order)
@@ -262,13 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_ffn_kernel(const MoEParams p)
     }
     __syncthreads();
     auto tok_row = [&](int slot) -> int { return slot_row[slot]; };
-    token_sigma(p.x, p.k, 0, p.k, SLOTS, tok_row, sigma);
-    __syncthreads();
+    stage_tokens<kMMA, SLOTS>(p.x, p.k, 0, p.kc, tok_row, s_amax, sigma, xs);
     if (threadIdx.x < SLOTS) {
       const float gsc = (e == kSharedSeg) ? __ldg(p.gs_sh) : __ldg(p.gs + e);
       mul[threadIdx.x] = gsc * exp2i(8 - sigma[threadIdx.x]);
     }
-    stage_x<kMMA, SLOTS>(p.x, p.k, 0, p.kc, tok_row, sigma, xs);
     __syncthreads();
 
     const int lo = run_lo(r);

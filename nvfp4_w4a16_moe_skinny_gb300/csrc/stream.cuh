@@ -141,74 +141,103 @@ __device__ __forceinline__ void ring_issue(const Ring& r, int s, const uint8_t* 
   bulk_g2s(r.buf + s * kStageBytes, src, bytes, &r.bar[s], policy);
 }
 
-// Stage the bf16 activations of `rows` token slots over columns [col0, col0 +
-// 64*nchunks) into shared memory as f16, each token rescaled by 2^sigma[slot].
+// Stage the bf16 activations of SLOTS token slots over columns [col0, col0 +
+// 64*nchunks) into shared memory as f16, each slot rescaled by 2^sigma[slot]
+// (sigma from the slot's amax over the same columns, see pow2_rescale_exponent).
 // tok_row(slot) gives the source row of x (or -1 for an empty slot); k = row length.
-// MMA layout (fragments) or CUDA-core layout (pairs), see the constants above.
+// Work items are (slot, 8-column group): one 16-byte load each, kStageBatch loads
+// in flight per thread.  Pass 1 takes the per-slot amax (shared-memory atomicMax
+// on the float bits, exact), pass 2 reloads (L1/L2 hits), converts and stores in
+// the MMA fragment layout or the CUDA-core pair layout (see the constants above).
+// All threads of the CTA call it; it ends with a __syncthreads.
+constexpr int kStageBatch = 8;
+
 template <bool kMMA, int SLOTS, typename TokRow>
-__device__ __forceinline__ void stage_x(const uint16_t* __restrict__ x, int k, int col0, int nchunks, TokRow tok_row,
-                                        const int* sigma, uint8_t* xs) {
-  uint32_t* xw = reinterpret_cast<uint32_t*>(xs);
-  if constexpr (kMMA) {
-    constexpr int NT = (SLOTS + 7) / 8;
-    const int words = nchunks * NT * 256;
-    for (int i = threadIdx.x; i < words; i += blockDim.x) {
-      const int kcl = i / (NT * 256);
-      const int rem = i - kcl * NT * 256;
-      const int nt = rem >> 8, ln = (rem >> 3) & 31, wd = rem & 7;
-      const int g = ln >> 2, t = ln & 3, kt = wd >> 1, hf = wd & 1;
-      const int slot = nt * 8 + g;
-      const int col = col0 + kcl * 64 + kt * 16 + 2 * t + 8 * hf;
-      uint32_t v = 0;
-      const int row = slot < SLOTS ? tok_row(slot) : -1;
-      if (row >= 0 && col < k) {
-        const uint32_t pair = __ldg(reinterpret_cast<const uint32_t*>(x + static_cast<size_t>(row) * k + col));
-        const float sc = exp2i(sigma[slot]);
-        const float lo = __uint_as_float(pair << 16) * sc, hi = __uint_as_float(pair & 0xFFFF0000u) * sc;
-        v = static_cast<uint32_t>(f32_to_f16_bits(lo)) | (static_cast<uint32_t>(f32_to_f16_bits(hi)) << 16);
-      }
-      xw[i] = v;
+__device__ __forceinline__ void stage_tokens(const uint16_t* __restrict__ x, int k, int col0, int nchunks,
+                                             TokRow tok_row, unsigned* s_amax, int* sigma, uint8_t* xs) {
+  const int groups = nchunks * 8;  // 8-column groups per slot
+  const int items = SLOTS * groups;
+  if (threadIdx.x < SLOTS) s_amax[threadIdx.x] = 0u;
+  __syncthreads();
+  auto src_of = [&](int it, int& slot, int& c8) -> const uint4* {
+    slot = it / groups;
+    c8 = it - slot * groups;
+    const int col = col0 + c8 * 8;
+    const int row = tok_row(slot);
+    if (row < 0 || col >= k) return nullptr;
+    return reinterpret_cast<const uint4*>(x + static_cast<size_t>(row) * k + col);
+  };
+  // ---- pass 1: amax per slot
+  for (int base = threadIdx.x; base < items; base += blockDim.x * kStageBatch) {
+    uint4 v[kStageBatch];
+    int sl[kStageBatch];
+#pragma unroll
+    for (int j = 0; j < kStageBatch; ++j) {
+      const int it = base + j * blockDim.x;
+      int c8;
+      const uint4* src = it < items ? src_of(it, sl[j], c8) : nullptr;
+      v[j] = src ? __ldg(src) : make_uint4(0, 0, 0, 0);
+      if (!src) sl[j] = -1;
     }
-  } else {
-    const int words = nchunks * SLOTS * 32;
-    for (int i = threadIdx.x; i < words; i += blockDim.x) {
-      const int kcl = i / (SLOTS * 32);
-      const int rem = i - kcl * SLOTS * 32;
-      const int slot = rem >> 5, pp = rem & 31;
-      const int col = col0 + kcl * 64 + 2 * pp;
-      uint32_t v = 0;
-      const int row = tok_row(slot);
-      if (row >= 0 && col < k) {
-        const uint32_t pair = __ldg(reinterpret_cast<const uint32_t*>(x + static_cast<size_t>(row) * k + col));
-        const float sc = exp2i(sigma[slot]);
-        const float lo = __uint_as_float(pair << 16) * sc, hi = __uint_as_float(pair & 0xFFFF0000u) * sc;
-        v = static_cast<uint32_t>(f32_to_f16_bits(lo)) | (static_cast<uint32_t>(f32_to_f16_bits(hi)) << 16);
-      }
-      xw[i] = v;
+#pragma unroll
+    for (int j = 0; j < kStageBatch; ++j) {
+      if (sl[j] < 0) continue;
+      const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+      float am = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        am = fmaxf(am, fmaxf(fabsf(__uint_as_float(w4[e] << 16)), fabsf(__uint_as_float(w4[e] & 0xFFFF0000u))));
+      if (am > 0.f) atomicMax(&s_amax[sl[j]], __float_as_uint(am));
     }
   }
-}
-
-// Per-slot power-of-two exponents from the amax of each token row over
-// columns [c0, c1): one warp per slot (slots <= warps per CTA).  Writes sigma[slot].
-template <typename TokRow>
-__device__ __forceinline__ void token_sigma(const uint16_t* __restrict__ x, int k, int c0, int c1, int slots,
-                                            TokRow tok_row, int* sigma) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int slot = warp; slot < slots; slot += blockDim.x >> 5) {
-    const int row = tok_row(slot);
-    float am = 0.f;
-    if (row >= 0) {
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(x + static_cast<size_t>(row) * k);
-      for (int c = c0 + 2 * lane; c < c1; c += 64) {
-        const uint32_t pair = __ldg(src + c / 2);
-        am = fmaxf(am, fmaxf(fabsf(__uint_as_float(pair << 16)), fabsf(__uint_as_float(pair & 0xFFFF0000u))));
+  __syncthreads();
+  if (threadIdx.x < SLOTS) sigma[threadIdx.x] = pow2_rescale_exponent(__uint_as_float(s_amax[threadIdx.x]));
+  __syncthreads();
+  // ---- pass 2: convert and store
+  uint32_t* xw = reinterpret_cast<uint32_t*>(xs);
+  for (int base = threadIdx.x; base < items; base += blockDim.x * kStageBatch) {
+    uint4 v[kStageBatch];
+    int sl[kStageBatch], cg[kStageBatch];
+#pragma unroll
+    for (int j = 0; j < kStageBatch; ++j) {
+      const int it = base + j * blockDim.x;
+      sl[j] = -1;
+      cg[j] = 0;
+      v[j] = make_uint4(0, 0, 0, 0);
+      if (it < items) {
+        // empty slots and columns past k are stored as zeros (the tile padding
+        // is zero too, but stale shared memory could hold non-finite values)
+        const uint4* src = src_of(it, sl[j], cg[j]);
+        if (src) v[j] = __ldg(src);
       }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
-    if (lane == 0) sigma[slot] = pow2_rescale_exponent(am);
+    for (int j = 0; j < kStageBatch; ++j) {
+      if (sl[j] < 0) continue;  // past the last item
+      const float sc = exp2i(sigma[sl[j]]);
+      const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+      uint32_t h[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = __uint_as_float(w4[e] << 16) * sc, hi = __uint_as_float(w4[e] & 0xFFFF0000u) * sc;
+        h[e] = static_cast<uint32_t>(f32_to_f16_bits(lo)) | (static_cast<uint32_t>(f32_to_f16_bits(hi)) << 16);
+      }
+      const int kcl = cg[j] >> 3, c64 = (cg[j] & 7) * 8;  // chunk, first column within the chunk
+      if constexpr (kMMA) {
+        constexpr int NT = (SLOTS + 7) / 8;
+        // columns c64..c64+7 = k-tile kt, half hf, pairs t = 0..3 -> lanes (g, t), word 2*kt + hf
+        const int kt = c64 >> 4, hf = (c64 >> 3) & 1;
+        const int nt = sl[j] >> 3, g = sl[j] & 7;
+        uint32_t* dst = xw + (static_cast<size_t>(kcl) * NT + nt) * 256 + (g * 4) * 8 + kt * 2 + hf;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) dst[t * 8] = h[t];
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(xw + (static_cast<size_t>(kcl) * SLOTS + sl[j]) * 32 + c64 / 2);
+        *dst = make_uint4(h[0], h[1], h[2], h[3]);
+      }
+    }
   }
+  __syncthreads();
 }
 
 }  // namespace nvfp4
