@@ -210,6 +210,32 @@ size_t lm_head_workspace_bytes(int32_t m, int32_t vocab);
 nvfp4_status lm_head_argmax(const nvfp4_weight *w, const uint16_t *x, int32_t m, float *max_logit,
                             int32_t *argmax, void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * lm_head_argmax without a caller-provided workspace.  The pages have no
+ * counterpart to this call: it exists for callers that cannot allocate device
+ * memory -- for example a plugin or runtime that hands the library only its
+ * input and output buffers from a fixed pool, or a decode loop that must not
+ * hit cudaMalloc's implicit device synchronisation or an out-of-memory failure
+ * in the middle of a request.
+ *
+ * Same arguments, result and limits as lm_head_argmax, minus ws/ws_bytes.  The
+ * scratch it needs (arrival counter + per-CTA partials, 135,168 bytes) is a
+ * static array inside this library's device code, so every GPU that loads the
+ * library holds it until the process exits.  No call allocates or frees memory.
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address with cudaGetSymbolAddress and zeroes it
+ *     (synchronously); make that first call before any stream capture.
+ *   - Every call clears the arrival counter on `stream` before its kernel; the
+ *     rest of the array keeps the last call's contents.
+ *   - All calls on a device share the one array: calls that may overlap on the
+ *     GPU (other streams, other host threads) race and give wrong results.
+ *     Serialise them, or use lm_head_argmax with separate workspaces.
+ *   - Returns NVFP4_ERR_WORKSPACE if lm_head_workspace_bytes(m, w->n) exceeds
+ *     the array (never for m <= 16 on a GPU with at most 1024 SMs).
+ */
+nvfp4_status lm_head_argmax_noalloc(const nvfp4_weight *w, const uint16_t *x, int32_t m, float *max_logit,
+                                    int32_t *argmax, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "nvfp4_skinny.h"
 #include "common.cuh"
@@ -375,3 +376,61 @@ nvfp4_status moe_ffn_grouped(const uint16_t* x, int32_t m, int32_t top_k, const 
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ lm_head without allocation
+// Scratch for lm_head_argmax_noalloc: the arrival counter (first 4 KiB) and the
+// per-CTA (value, row) partials for up to 1024 CTAs x 16 tokens.  It lives in
+// the library's own device memory, so callers pass only inputs and outputs.
+namespace nvfp4 {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = kCounterBytes + static_cast<size_t>(1024) * 16 * (sizeof(float) + sizeof(int));
+static __device__ __align__(256) uint8_t g_lm_head_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch array on the current device.  The first call on a
+// device looks it up (the host-side name of the array is not a device address)
+// and zeroes it once; later calls reuse the cached address.
+nvfp4_status scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_lm_head_scratch) != cudaSuccess || !ptr) return NVFP4_ERR_CUDA;
+    if (cudaMemset(ptr, 0, kNoAllocScratchBytes) != cudaSuccess) return NVFP4_ERR_CUDA;
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return NVFP4_OK;
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" nvfp4_status lm_head_argmax_noalloc(const nvfp4_weight* w, const uint16_t* x, int32_t m, float* max_logit,
+                                               int32_t* argmax, cudaStream_t stream) {
+  if (const nvfp4_status st = check_weight(w, 1, 0)) return st;
+  if (!x || !max_logit || !argmax) return NVFP4_ERR_NULL;
+  if (m < 1 || m > 16) return NVFP4_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(max_logit, 4) || !aligned(argmax, 4)) return NVFP4_ERR_ALIGN;
+  if (lm_head_workspace_bytes(m, w->n) > kNoAllocScratchBytes) return NVFP4_ERR_WORKSPACE;
+  void* ws = nullptr;
+  if (const nvfp4_status st = scratch_address(&ws)) return st;
+  // the arrival counter must read zero when the kernel starts
+  if (cudaMemsetAsync(ws, 0, sizeof(unsigned), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+  SkinnyParams p{};
+  p.w = static_cast<const uint8_t*>(w->data);
+  p.gscale = w->global_scale;
+  p.x = x;
+  p.m = m, p.n = w->n, p.k = w->k;
+  p.nb = ceil_div(w->n, kTileRows), p.kc = ceil_div(w->k, kTileK);
+  p.counters = static_cast<unsigned*>(ws);
+  p.am_val = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes);
+  p.am_idx = reinterpret_cast<int*>(p.am_val + 1024 * m);
+  p.max_logit = max_logit;
+  p.argmax = argmax;
+  return dispatch_skinny<kEpiArgmax>(p, false, stream);
+}
