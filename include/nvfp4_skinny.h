@@ -148,11 +148,12 @@ nvfp4_status nvfp4_repack(const uint8_t *nibbles, const uint8_t *scales, int32_t
  *   w   num_matrices == 1, flags == 0.
  *   x   (device) bf16 [m, w->k], 16-byte aligned.
  *   y   (device) bf16 [m, w->n], 4-byte aligned.
- *   ws  (device) nvfp4_gemm_workspace_bytes(m, n, k) bytes, 16-byte aligned
- *       (may be NULL when that is 0).  Its first 4 KiB hold arrival counters
- *       that must be zero before the first call that uses this workspace (for
- *       example cudaMemsetAsync once after allocation); every call leaves them
- *       consistent for the next.
+ *   ws  (device) nvfp4_gemm_workspace_bytes(m, n, k) bytes, 16-byte aligned.
+ *       It holds the k-split fixup area: 64 KiB of arrival counters, then the
+ *       partial sums.  The counters must be zero before the first call that
+ *       uses this workspace (for example cudaMemsetAsync once after
+ *       allocation); every completed call leaves them zero again, so the same
+ *       workspace may serve calls of any shape whose size it covers.
  * M = 1..7 runs on CUDA cores (warp-shuffle reduction); M = 8..16 on m16n8k16
  * tensor-core MMAs with the weights as the 16-row operand.
  */
@@ -187,10 +188,16 @@ nvfp4_status moe_route_topk(const float *logits, int32_t m, int32_t n_experts, i
  *   down            stacked [E, d, inter], flags 0.
  *   shared_gate_up, shared_down: one matrix each of the same shapes, or both NULL.
  *   out             (device) bf16 [m, d].
- *   ws              (device) moe_ffn_workspace_bytes(m, top_k, d, inter) bytes.
- * Limits: 1 <= m <= 4096, d % 64 == 0, inter % 64 == 0.
+ *   ws              (device) moe_ffn_workspace_bytes(m, top_k, E, d, inter) bytes,
+ *                   16-byte aligned.  It holds h, the per-(token, slot) down
+ *                   outputs and a k-split fixup area (64 KiB of arrival counters,
+ *                   then partial sums).  The counters must be zero before the
+ *                   first call on this workspace (for example cudaMemsetAsync
+ *                   once after allocation); every completed call leaves them
+ *                   zero again.
+ * Limits: 1 <= m <= 16, d % 64 == 0, inter % 64 == 0.
  */
-size_t moe_ffn_workspace_bytes(int32_t m, int32_t top_k, int32_t d, int32_t inter);
+size_t moe_ffn_workspace_bytes(int32_t m, int32_t top_k, int32_t n_experts, int32_t d, int32_t inter);
 nvfp4_status moe_ffn_grouped(const uint16_t *x, int32_t m, int32_t top_k, const float *probs,
                              const int32_t *expert_offsets, const int32_t *sorted_pairs,
                              const nvfp4_weight *gate_up, const nvfp4_weight *down,

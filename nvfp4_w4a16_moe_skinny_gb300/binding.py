@@ -82,7 +82,7 @@ def _sig(lib):
     lib.nvfp4_gemm.argtypes = [ctypes.POINTER(CWeight), _P, _I, _P, _P, _SZ, _P]
     lib.moe_route_topk.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P]
     lib.moe_ffn_workspace_bytes.restype = _SZ
-    lib.moe_ffn_workspace_bytes.argtypes = [_I, _I, _I, _I]
+    lib.moe_ffn_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
     lib.moe_ffn_grouped.argtypes = [_P, _I, _I, _P, _P, _P, ctypes.POINTER(CWeight), ctypes.POINTER(CWeight),
                                     ctypes.POINTER(CWeight), ctypes.POINTER(CWeight), _P, _P, _SZ, _P]
     lib.lm_head_workspace_bytes.restype = _SZ
@@ -218,7 +218,7 @@ class Library:
         inter = down.k
         if out is None:
             out = torch.empty((m, d), dtype=torch.bfloat16, device=x.device)
-        nbytes = self.lib.moe_ffn_workspace_bytes(m, top_k, d, inter)
+        nbytes = self.lib.moe_ffn_workspace_bytes(m, top_k, gate_up.num_matrices, d, inter)
         ws = self.workspace("moe", nbytes, x.device)
         cg, cd = gate_up.c(), down.c()
         sg = ctypes.byref(shared_gate_up.c()) if shared_gate_up is not None else None
@@ -266,7 +266,8 @@ class Library:
         m, d = x.shape
         e = logits.shape[1]
         ids, probs, offsets, pairs = route_out
-        ws = self.workspace("moe", self.lib.moe_ffn_workspace_bytes(m, top_k, d, down.k), x.device)
+        ws = self.workspace("moe", self.lib.moe_ffn_workspace_bytes(m, top_k, gate_up.num_matrices, d, down.k),
+                            x.device)
         cg, cd = gate_up.c(), down.c()
         sg = shared_gate_up.c() if shared_gate_up is not None else None
         sd = shared_down.c() if shared_down is not None else None

@@ -13,6 +13,7 @@
 namespace nvfp4 {
 
 constexpr int kTileRows = 16;       // rows per repacked tile
+constexpr int kGroupRows = 64;      // rows per group of four tiles (the streaming unit)
 constexpr int kTileK = 64;          // K columns per repacked tile
 constexpr int kTileBytes = 576;     // 512 B of nibbles + 64 B of scales
 constexpr int kTileNibBytes = 512;
@@ -59,16 +60,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete sleeps
+// in hardware until the phase completes or about `ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded warp-collective wait (all 32 lanes call it) for the phase with the
 // given parity to complete.  Every lane observes the completion itself (so the
 // bulk-copied bytes are visible to it) and all lanes return the same answer:
 // false, with kErrWaitTimeout recorded, if the phase did not complete within
 // kWaitCycles.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
-  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, 1u << 20))) return true;
   const long long t0 = clock64();
   while (true) {
-    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, 1u << 20))) return true;
     if (__any_sync(0xffffffffu, clock64() - t0 > kWaitCycles)) {
       if ((threadIdx.x & 31) == 0) atomicOr(&g_device_error, kErrWaitTimeout);
       return false;

@@ -1,33 +1,38 @@
-// Per-warp weight streaming and the two tile consumers (sm_103a).
+// Per-warp weight streaming and the chunk consumers (sm_103a).
 //
-// Every warp owns a private ring of `ns` stages in shared memory.  Lane 0 fills
-// a stage with one 1-D bulk copy (TMA engine, L2 evict-first) of a contiguous
-// run of up to kTPS 576-byte tiles; the whole warp waits on the stage's
-// mbarrier; when the warp has consumed a stage, lane 0 refills it with the
-// chunk `ns` positions ahead.  No stage is shared between warps, so the only
-// synchronisation is the mbarrier (copy -> warp) and __syncwarp (warp -> refill).
+// A *chunk* is the four 576-byte tiles of one 64-row group and one 64-column
+// slice of K (2,304 contiguous bytes in the repacked layout, version 2).  Every
+// warp owns a private ring of `ns` chunk-sized stages in shared memory.  Lane 0
+// fills a stage with one 1-D bulk copy (TMA engine, L2 evict-first); the whole
+// warp waits on the stage's mbarrier; when the warp has consumed a stage, lane 0
+// refills it with the chunk `ns` positions ahead.  No stage is shared between
+// warps, so the only synchronisation is the mbarrier (copy -> warp) and
+// __syncwarp (warp -> refill).
 //
-// Tile consumers:
-//  * mma_tile<NT>: tensor cores (m16n8k16, f16 in, f32 accumulate); weights are
-//    the 16-row A operand and up to 8*NT tokens the N operand.  One 16-byte
-//    shared load per lane yields the A fragments of four 16-column groups; each
-//    E2M1 pair goes through the hardware converter and is multiplied in f16 by
-//    its E4M3 scale (exact: the product has at most 6 significant bits).
-//  * core_tile<MT>: CUDA cores for up to 7 tokens.  Lane (g, q) takes rows g and
-//    g+8 over 16-column group q of the tile; it sums E2M1 x activation products
-//    in f32 (mixed-precision FMA; the products are exact), scales each group
-//    sum once, and the cross-lane reduction is left to warp shuffles.
+// Chunk consumers:
+//  * mma_chunk<NT>: tensor cores (m16n8k16, f16 in, f32 accumulate); each tile's
+//    16 rows are the A operand and up to 8*NT tokens the N operand.  The x
+//    fragments of the 64 columns are loaded once and feed the four tiles, which
+//    also gives four independent accumulator chains.  Each E2M1 pair goes
+//    through the hardware converter and is multiplied in f16 by its E4M3 scale
+//    (exact: the product has at most 6 significant bits).
+//  * core_chunk<MT>: CUDA cores for up to 7 tokens.  Lane (g, q) takes rows g and
+//    g+8 of each tile over the 16-column group q; it sums E2M1 x activation
+//    products in f32 (mixed-precision FMA; the products are exact) and scales
+//    each group sum once (MT <= 2), or scales the weights in f16 first and
+//    accumulates directly (MT >= 3, fewer live registers).  The cross-lane sum
+//    over q is left to warp shuffles in the epilogue.
 #pragma once
 
 #include "common.cuh"
 
 namespace nvfp4 {
 
-constexpr int kTPS = 4;  // tiles per ring stage (2304 bytes)
-constexpr int kStageBytes = kTPS * kTileBytes;
+constexpr int kChunkTiles = 4;                          // tiles per chunk (one 64-row group)
+constexpr int kStageBytes = kChunkTiles * kTileBytes;   // 2,304 bytes
 
 // x fragments for the MMA path, per 64-column chunk and 8-token group: 32 lanes x
-// 8 words (f16x2).  Lane (g, t), word 2*kt + h holds tokens slot g, columns
+// 8 words (f16x2).  Lane (g, t), word 2*kt + h holds token slot g, columns
 // 16*kt + 2*t + 8*h (+1) of the chunk -- the m16n8k16 B fragment.
 constexpr int kXFragChunkBytes = 1024;
 // x for the CUDA-core path, per 64-column chunk and token: 32 f16x2 words (pairs).
@@ -47,31 +52,40 @@ __device__ __forceinline__ void mma_step(uint32_t word, uint32_t sg, uint32_t sg
   for (int nt = 0; nt < NT; ++nt) mma_f16(acc[nt], a, b0[nt], b1[nt]);
 }
 
-// One 16x64 tile against x fragments `xf` (NT * 1024 bytes for this chunk).
-// acc[nt] is the C fragment: [0],[1] = row g, tokens 8nt+2t, +1; [2],[3] = row g+8.
+// One chunk (4 tiles at `st`) against x fragments `xf` (NT * 1024 bytes).
+// acc[r][nt] is tile r's C fragment: [0],[1] = row g, tokens 8nt+2t, +1; [2],[3] = row g+8.
 template <int NT>
-__device__ __forceinline__ void mma_tile(const uint8_t* tile, const uint8_t* xf, int lane, float (&acc)[NT][4]) {
-  const uint4 wv = lds128(tile + lane * 16);
-  const uint2 sv = lds64(tile + kTileNibBytes + (lane >> 2) * 8);
+__device__ __forceinline__ void mma_chunk(const uint8_t* st, const uint8_t* xf, int lane, float (&acc)[4][NT][4]) {
   uint4 xa[NT], xb[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     xa[nt] = lds128(xf + nt * kXFragChunkBytes + lane * 32);
     xb[nt] = lds128(xf + nt * kXFragChunkBytes + lane * 32 + 16);
   }
+  uint4 wv[4];
+  uint2 sv[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    wv[r] = lds128(st + r * kTileBytes + lane * 16);
+    sv[r] = lds64(st + r * kTileBytes + kTileNibBytes + (lane >> 2) * 8);
+  }
   uint32_t b0[NT], b1[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) b0[nt] = xa[nt].x, b1[nt] = xa[nt].y;
-  mma_step<NT>(wv.x, scale_pair_x2<0>(sv.x), scale_pair_x2<1>(sv.x), b0, b1, acc);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) mma_step<NT>(wv[r].x, scale_pair_x2<0>(sv[r].x), scale_pair_x2<1>(sv[r].x), b0, b1, acc[r]);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) b0[nt] = xa[nt].z, b1[nt] = xa[nt].w;
-  mma_step<NT>(wv.y, scale_pair_x2<2>(sv.x), scale_pair_x2<3>(sv.x), b0, b1, acc);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) mma_step<NT>(wv[r].y, scale_pair_x2<2>(sv[r].x), scale_pair_x2<3>(sv[r].x), b0, b1, acc[r]);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) b0[nt] = xb[nt].x, b1[nt] = xb[nt].y;
-  mma_step<NT>(wv.z, scale_pair_x2<0>(sv.y), scale_pair_x2<1>(sv.y), b0, b1, acc);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) mma_step<NT>(wv[r].z, scale_pair_x2<0>(sv[r].y), scale_pair_x2<1>(sv[r].y), b0, b1, acc[r]);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) b0[nt] = xb[nt].z, b1[nt] = xb[nt].w;
-  mma_step<NT>(wv.w, scale_pair_x2<2>(sv.y), scale_pair_x2<3>(sv.y), b0, b1, acc);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) mma_step<NT>(wv[r].w, scale_pair_x2<2>(sv[r].y), scale_pair_x2<3>(sv[r].y), b0, b1, acc[r]);
 }
 
 __device__ __forceinline__ uint32_t lds_u16(const void* p) {
@@ -80,42 +94,106 @@ __device__ __forceinline__ uint32_t lds_u16(const void* p) {
   return v;
 }
 
-// One 16x64 tile on CUDA cores.  xw: the chunk's x words [MT][32] (pair pp =
-// columns 2pp, 2pp+1).  acc[m][0] = row g, acc[m][1] = row g+8 (partial over
-// this lane's group q; summed over q by the caller).
-template <int MT>
-__device__ __forceinline__ void core_tile(const uint8_t* tile, const uint8_t* xw, int g, int q, float (&acc)[MT][2]) {
-  const uint32_t sp = scale_lohi_x2(lds_u16(tile + kTileNibBytes + 8 * g + 2 * q));
-  const float sg = f16lo_to_f32(sp), sg8 = f16hi_to_f32(sp);  // scale * 2^-8
-  const int h = g >> 1;
-  float pa[MT], pb[MT], pc[MT], pd[MT];
+// Per-lane constants of the CUDA-core consumer: lane (g, q) reads, at step j, the
+// 32-bit word q of lane-chunk t_j = (j + g/2) & 3 of row pair g (the rotation by
+// g/2 puts the 32 lanes on 32 distinct banks) and the x pairs 8q + t_j, 8q + t_j + 4.
+struct CoreLane {
+  int w_off[4];   // byte offset of the weight word within a tile
+  int x_off[4];   // byte offset of x pair 8q + t_j within a token's 64-column chunk
+  int s_off;      // byte offset of the scale pair (rows g, g+8; group q) within a tile
+  __device__ __forceinline__ CoreLane(int lane) {
+    const int g = lane >> 2, q = lane & 3;
 #pragma unroll
-  for (int m = 0; m < MT; ++m) pa[m] = pb[m] = pc[m] = pd[m] = 0.f;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    // rotate the 4 lane-chunks by g/2 so the 32 lanes hit 32 distinct banks
-    const int t = (j + h) & 3;
-    const uint32_t word = lds32(tile + 16 * (4 * g + t) + 4 * q);
-    uint32_t hh[4];
-    e2m1x8_to_f16x2(word, hh);
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      const uint32_t x0 = lds32(xw + m * kXCoreChunkBytes + (8 * q + t) * 4);
-      const uint32_t x1 = lds32(xw + m * kXCoreChunkBytes + (8 * q + t + 4) * 4);
-      pa[m] = fma_f16lo(hh[0], x0, pa[m]);
-      pb[m] = fma_f16hi(hh[0], x0, pb[m]);
-      pa[m] = fma_f16lo(hh[2], x1, pa[m]);
-      pb[m] = fma_f16hi(hh[2], x1, pb[m]);
-      pc[m] = fma_f16lo(hh[1], x0, pc[m]);
-      pd[m] = fma_f16hi(hh[1], x0, pd[m]);
-      pc[m] = fma_f16lo(hh[3], x1, pc[m]);
-      pd[m] = fma_f16hi(hh[3], x1, pd[m]);
+    for (int j = 0; j < 4; ++j) {
+      const int t = (j + (g >> 1)) & 3;
+      w_off[j] = 16 * (4 * g + t) + 4 * q;
+      x_off[j] = (8 * q + t) * 4;
     }
+    s_off = kTileNibBytes + 8 * g + 2 * q;
   }
+};
+
+// One chunk on CUDA cores.  xw: the chunk's x words [MT][32 words].  acc[r][m][0]
+// = tile r, row g; acc[r][m][1] = row g+8 (partial over this lane's group q).
+template <int MT>
+__device__ __forceinline__ void core_chunk(const uint8_t* st, const uint8_t* xw, const CoreLane& cl,
+                                           float (&acc)[4][MT][2]) {
+  if constexpr (MT <= 2) {
+    uint32_t xr[MT][4][2];
 #pragma unroll
-  for (int m = 0; m < MT; ++m) {
-    acc[m][0] = fmaf(pa[m] + pb[m], sg, acc[m][0]);
-    acc[m][1] = fmaf(pc[m] + pd[m], sg8, acc[m][1]);
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        xr[m][j][0] = lds32(xw + m * kXCoreChunkBytes + cl.x_off[j]);
+        xr[m][j][1] = lds32(xw + m * kXCoreChunkBytes + cl.x_off[j] + 16);
+      }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint8_t* tile = st + r * kTileBytes;
+      const uint32_t sp = scale_lohi_x2(lds_u16(tile + cl.s_off));
+      float pa[MT], pb[MT], pc[MT], pd[MT];
+#pragma unroll
+      for (int m = 0; m < MT; ++m) pa[m] = pb[m] = pc[m] = pd[m] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t hh[4];
+        e2m1x8_to_f16x2(lds32(tile + cl.w_off[j]), hh);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          pa[m] = fma_f16lo(hh[0], xr[m][j][0], pa[m]);
+          pb[m] = fma_f16hi(hh[0], xr[m][j][0], pb[m]);
+          pa[m] = fma_f16lo(hh[2], xr[m][j][1], pa[m]);
+          pb[m] = fma_f16hi(hh[2], xr[m][j][1], pb[m]);
+          pc[m] = fma_f16lo(hh[1], xr[m][j][0], pc[m]);
+          pd[m] = fma_f16hi(hh[1], xr[m][j][0], pd[m]);
+          pc[m] = fma_f16lo(hh[3], xr[m][j][1], pc[m]);
+          pd[m] = fma_f16hi(hh[3], xr[m][j][1], pd[m]);
+        }
+      }
+      const float sg = f16lo_to_f32(sp), sg8 = f16hi_to_f32(sp);  // scale * 2^-8
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        acc[r][m][0] = fmaf(pa[m] + pb[m], sg, acc[r][m][0]);
+        acc[r][m][1] = fmaf(pc[m] + pd[m], sg8, acc[r][m][1]);
+      }
+    }
+  } else {
+    uint32_t sgd[4], sg8d[4];  // (scale, scale) * 2^-8 per tile for rows g and g+8
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint32_t sw = lds_u16(st + r * kTileBytes + cl.s_off);
+      sgd[r] = scale_pair_x2<0>(sw);
+      sg8d[r] = scale_pair_x2<1>(sw);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t x0[MT], x1[MT];
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        x0[m] = lds32(xw + m * kXCoreChunkBytes + cl.x_off[j]);
+        x1[m] = lds32(xw + m * kXCoreChunkBytes + cl.x_off[j] + 16);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        uint32_t hh[4];
+        e2m1x8_to_f16x2(lds32(st + r * kTileBytes + cl.w_off[j]), hh);
+        const uint32_t h0 = hmul2(hh[0], sgd[r]), h2 = hmul2(hh[2], sgd[r]);
+        const uint32_t h1 = hmul2(hh[1], sg8d[r]), h3 = hmul2(hh[3], sg8d[r]);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          float a0 = acc[r][m][0], a1 = acc[r][m][1];
+          a0 = fma_f16lo(h0, x0[m], a0);
+          a0 = fma_f16hi(h0, x0[m], a0);
+          a0 = fma_f16lo(h2, x1[m], a0);
+          a0 = fma_f16hi(h2, x1[m], a0);
+          a1 = fma_f16lo(h1, x0[m], a1);
+          a1 = fma_f16hi(h1, x0[m], a1);
+          a1 = fma_f16lo(h3, x1[m], a1);
+          a1 = fma_f16hi(h3, x1[m], a1);
+          acc[r][m][0] = a0, acc[r][m][1] = a1;
+        }
+      }
+    }
   }
 }
 
@@ -134,11 +212,10 @@ __device__ __forceinline__ void ring_init(const Ring& r, int lane) {
   __syncwarp();
 }
 
-// Lane 0 only: copy `ntiles` tiles from `src` into stage s.
-__device__ __forceinline__ void ring_issue(const Ring& r, int s, const uint8_t* src, int ntiles, uint64_t policy) {
-  const uint32_t bytes = static_cast<uint32_t>(ntiles * kTileBytes);
-  mbar_arrive_expect_tx(&r.bar[s], bytes);
-  bulk_g2s(r.buf + s * kStageBytes, src, bytes, &r.bar[s], policy);
+// Lane 0 only: copy the chunk at `src` (kStageBytes) into stage s.
+__device__ __forceinline__ void ring_issue(const Ring& r, int s, const uint8_t* src, uint64_t policy) {
+  mbar_arrive_expect_tx(&r.bar[s], kStageBytes);
+  bulk_g2s(r.buf + s * kStageBytes, src, kStageBytes, &r.bar[s], policy);
 }
 
 // Stage the bf16 activations of SLOTS token slots over columns [col0, col0 +

@@ -4,22 +4,25 @@ The pages say only that weights are repacked once, offline, "into
 mma-fragment order" so kernel loads are 16-byte coalesced
 (gemma-cuda-hybrid README, "Everything it has / Inference engine" and
 "NVFP4-specific").  The layout itself is this library's; its specification
-(restated in DESIGN.md, "Data layout in HBM") is:
+(restated in DESIGN.md, "Data layout in HBM") is, for layout version 2:
 
-* Rows are padded to a multiple of 16, K to a multiple of 64, with zero bytes.
-* A *gated* matrix [gate || up] with N = 2I (I % 8 == 0) first has its rows
+* Rows are padded to a multiple of 64, K to a multiple of 64, with zero bytes.
+* A *gated* matrix [gate || up] with N = 2I (I % 32 == 0) first has its rows
   permuted: gate row i goes to row 16*(i//8) + i%8, up row i to
   16*(i//8) + 8 + i%8, so each 16-row block holds 8 gate rows and the 8 up rows
   of the same indices.
-* The padded matrix is cut into tiles of 16 rows x 64 columns; tile (rb, kc)
-  starts at byte 576 * (rb * KC + kc), KC = K_pad / 64.  A stack of E matrices
-  puts matrix e at byte e * (NB * KC * 576), NB = N_pad / 16.
-* Tile bytes [0, 512): byte 16*lane + 4*kt + r with lane = 4*g + t
-  (g in 0..7, t in 0..3, kt in 0..3, r in 0..3) is the canonical byte holding
-  columns (c, c+1) of row R, where R = 16*rb + g + 8*(r & 1) and
-  c = 64*kc + 16*kt + 2*t + 8*(r >> 1); low nibble = column c.
-* Tile bytes [512, 576): byte 512 + 8*g + 2*kt + h is the scale of row
-  16*rb + g + 8*h, group 4*kc + kt.
+* The padded matrix is cut into tiles of 16 rows x 64 columns.  Four
+  consecutive 16-row blocks form a 64-row group; tile (group G, chunk kc,
+  block r in 0..3) starts at byte 576 * ((G * KC + kc) * 4 + r), KC = K_pad / 64:
+  the four tiles of one group and one 64-column chunk are contiguous (2,304 B).
+  A stack of E matrices puts matrix e at byte e * (NG * KC * 4 * 576),
+  NG = N_pad / 64.
+* Tile bytes [0, 512): byte 16*lane + 4*kt + r (lane = 4*g + t, g in 0..7,
+  t in 0..3, kt in 0..3, r in 0..3) is the canonical byte holding columns
+  (c, c+1) of the tile's row g + 8*(r & 1), with c = 64*kc + 16*kt + 2*t +
+  8*(r >> 1); low nibble = column c.
+* Tile bytes [512, 576): byte 512 + 8*g + 2*kt + h is the scale of the tile's
+  row g + 8*h, group 4*kc + kt.
 
 This module computes the same mapping independently of the CUDA repack kernel:
 for every (row, column pair) and (row, group) it places the canonical byte.
@@ -30,19 +33,20 @@ from __future__ import annotations
 import numpy as np
 
 TILE_ROWS = 16
+GROUP_ROWS = 64
 TILE_COLS = 64
 TILE_BYTES = 576
 
 
 def padded_dims(n: int, k: int):
-    n_pad = -(-n // TILE_ROWS) * TILE_ROWS
+    n_pad = -(-n // GROUP_ROWS) * GROUP_ROWS
     k_pad = -(-k // TILE_COLS) * TILE_COLS
     return n_pad, k_pad
 
 
 def repacked_bytes(n: int, k: int, num_matrices: int = 1) -> int:
     n_pad, k_pad = padded_dims(n, k)
-    return num_matrices * (n_pad // 16) * (k_pad // 64) * TILE_BYTES
+    return num_matrices * (n_pad // TILE_ROWS) * (k_pad // TILE_COLS) * TILE_BYTES
 
 
 def row_permutation(n: int, gated: bool) -> np.ndarray:
@@ -56,11 +60,17 @@ def row_permutation(n: int, gated: bool) -> np.ndarray:
     return 16 * (i // 8) + 8 * half + i % 8
 
 
+def _tile_start(dest_row, kc, kc_count):
+    rb = dest_row // 16
+    grp, r = rb // 4, rb % 4
+    return TILE_BYTES * ((grp * kc_count + kc) * 4 + r)
+
+
 def nibble_byte_offset(dest_row, col_pair, kc_count):
     """Byte offset (within one matrix) of the canonical byte (dest_row, column pair col_pair)."""
     dest_row = np.asarray(dest_row, np.int64)
     c = 2 * np.asarray(col_pair, np.int64)
-    rb, rr = dest_row // 16, dest_row % 16
+    rr = dest_row % 16
     kc, cc = c // 64, c % 64
     g, hrow = rr % 8, rr // 8
     kt, c16 = cc // 16, cc % 16
@@ -68,16 +78,16 @@ def nibble_byte_offset(dest_row, col_pair, kc_count):
     t = t2 // 2
     r = hrow + 2 * hcol
     lane = 4 * g + t
-    return TILE_BYTES * (rb * kc_count + kc) + 16 * lane + 4 * kt + r
+    return _tile_start(dest_row, kc, kc_count) + 16 * lane + 4 * kt + r
 
 
 def scale_byte_offset(dest_row, group, kc_count):
     dest_row = np.asarray(dest_row, np.int64)
     grp = np.asarray(group, np.int64)
-    rb, rr = dest_row // 16, dest_row % 16
+    rr = dest_row % 16
     kc, kt = grp // 4, grp % 4
     g, h = rr % 8, rr // 8
-    return TILE_BYTES * (rb * kc_count + kc) + 512 + 8 * g + 2 * kt + h
+    return _tile_start(dest_row, kc, kc_count) + 512 + 8 * g + 2 * kt + h
 
 
 def repack(nib: np.ndarray, scales: np.ndarray, gated: bool = False) -> np.ndarray:

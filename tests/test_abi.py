@@ -49,7 +49,8 @@ def test_status_strings_and_version(so):
         assert so.nvfp4_status_string(code) == text
 
 
-@pytest.mark.parametrize("n,k,e", [(16, 64, 1), (40, 80, 2), (262144, 2816, 1), (1408, 2816, 128), (1, 16, 1)])
+@pytest.mark.parametrize("n,k,e", [(16, 64, 1), (40, 80, 2), (262144, 2816, 1), (1408, 2816, 128), (1, 16, 1),
+                                   (2816, 704, 128), (200, 320, 3)])
 def test_repacked_bytes_matches_layout_spec(so, n, k, e):
     assert so.nvfp4_repacked_bytes(n, k, e) == OL.repacked_bytes(n, k, e)
 
@@ -59,7 +60,9 @@ def test_sizes_reject_bad_shapes(so):
     assert so.nvfp4_repacked_bytes(0, 64, 1) == 0
     assert so.nvfp4_gemm_workspace_bytes(17, 64, 64) == 0   # m > 16
     assert so.lm_head_workspace_bytes(0, 100) == 0
-    assert so.moe_ffn_workspace_bytes(15, 8, 2816, 704) == (15 * 8 + 15) * (704 * 2 + 2816 * 4)
+    assert so.moe_ffn_workspace_bytes(17, 8, 128, 2816, 704) == 0        # m > 16
+    # h (bf16) and the per-(token, slot) down outputs (fp32) are always part of it
+    assert so.moe_ffn_workspace_bytes(15, 8, 128, 2816, 704) >= (15 * 8 + 15) * (704 * 2 + 2816 * 4)
 
 
 def _weight(data=1 << 20, gs=1 << 20, n=64, k=64, e=1, flags=0, version=1):
@@ -83,8 +86,10 @@ def test_gemm_argument_errors_return_before_any_launch(so):
     assert so.nvfp4_gemm(ctypes.byref(w), x, 0, y, ws, 1 << 20, None) == 2
     assert so.nvfp4_gemm(ctypes.byref(w), x, 17, y, ws, 1 << 20, None) == 2
     assert so.nvfp4_gemm(ctypes.byref(w), ctypes.c_void_p((1 << 20) + 8), 1, y, ws, 1 << 20, None) == 3
-    assert so.nvfp4_gemm(ctypes.byref(w), x, 1, y, ws, 16, None) == 4
     assert so.nvfp4_gemm(ctypes.byref(w), x, 1, y, None, 1 << 20, None) == 4
+    big = _weight(n=4096, k=4096)                     # small N splits K: the fixup area is needed
+    assert so.nvfp4_gemm_workspace_bytes(16, 4096, 4096) > 1 << 20
+    assert so.nvfp4_gemm(ctypes.byref(big), x, 16, y, ws, 16, None) == 4
     w = _weight(data=(1 << 20) + 4)
     assert so.nvfp4_gemm(ctypes.byref(w), x, 1, y, ws, 1 << 20, None) == 3
 

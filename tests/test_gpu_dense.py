@@ -64,7 +64,7 @@ def test_quantizer_stacked(lib):
 # ------------------------------------------------------------------ repack
 
 @pytest.mark.parametrize("e,n,k,gated", [(1, 16, 64, False), (2, 40, 80, False), (1, 1000, 320, False),
-                                         (3, 32, 128, True), (2, 48, 16, True)])
+                                         (3, 64, 128, True), (2, 128, 16, True), (1, 1408, 2816, True)])
 def test_repack_bytes_bit_exact(lib, e, n, k, gated):
     rng = np.random.default_rng(n * 7 + k)
     nib = rng.integers(0, 256, (e, n, k // 2), dtype=np.uint8)

@@ -178,7 +178,7 @@ def test_lm_head_argmax_brute_force_planted_max_and_ties():
 
 def test_layout_round_trip_and_padding():
     rng = np.random.default_rng(7)
-    for (n, k, gated) in [(16, 64, False), (40, 80, False), (32, 128, True), (48, 16, True)]:
+    for (n, k, gated) in [(16, 64, False), (40, 80, False), (64, 128, True), (128, 16, True), (200, 320, False)]:
         nib = rng.integers(0, 256, (2, n, k // 2), dtype=np.uint8)
         sc = rng.integers(0, 127, (2, n, k // 16), dtype=np.uint8)
         buf = L.repack(nib, sc, gated)
@@ -197,10 +197,8 @@ def test_layout_round_trip_and_padding():
 
 
 def test_layout_hand_checked_positions():
-    """Byte positions worked out by hand from the layout specification."""
-    n, k = 32, 128
-    nib = np.arange(n * k // 2, dtype=np.int64).reshape(n, k // 2)
-    # tile (0,0): lane 0 word 0 = (row0,c0-1), (row8,c0-1), (row0,c8-9), (row8,c8-9)
+    """Byte positions worked out by hand from the layout specification (version 2)."""
+    # tile (group 0, chunk 0, block 0): lane 0 word 0 = (row0,c0-1), (row8,c0-1), (row0,c8-9), (row8,c8-9)
     assert L.nibble_byte_offset(0, 0, 2) == 0
     assert L.nibble_byte_offset(8, 0, 2) == 1
     assert L.nibble_byte_offset(0, 4, 2) == 2
@@ -211,15 +209,20 @@ def test_layout_hand_checked_positions():
     assert L.nibble_byte_offset(0, 8, 2) == 4
     # row 1 is g = 1 -> lane 4 -> byte 64
     assert L.nibble_byte_offset(1, 0, 2) == 64
-    # second 64-column chunk is the next tile; second row block is two tiles further
-    assert L.nibble_byte_offset(0, 32, 2) == 576
-    assert L.nibble_byte_offset(16, 0, 2) == 2 * 576
+    # rows 16..31 are block 1 of group 0: the next tile of the same chunk
+    assert L.nibble_byte_offset(16, 0, 2) == 576
+    assert L.nibble_byte_offset(48, 0, 2) == 3 * 576
+    # columns 64..127 are chunk 1: after the 4 tiles of chunk 0
+    assert L.nibble_byte_offset(0, 32, 2) == 4 * 576
+    # rows 64.. are group 1: after both chunks (2 x 4 tiles) of group 0
+    assert L.nibble_byte_offset(64, 0, 2) == 8 * 576
     # scales: row 0 group 0 at 512, row 8 group 0 at 513, row 0 group 1 at 514, row 1 at 520
-    assert [int(L.scale_byte_offset(r, gg, 2)) for r, gg in [(0, 0), (8, 0), (0, 1), (1, 0), (0, 4)]] == [512, 513, 514, 520, 576 + 512]
+    assert [int(L.scale_byte_offset(r, gg, 2)) for r, gg in [(0, 0), (8, 0), (0, 1), (1, 0), (0, 4), (16, 0)]] == \
+        [512, 513, 514, 520, 4 * 576 + 512, 576 + 512]
     # gated: gate row 9 -> block 1 row 1; up row 9 -> block 1 row 9
     perm = L.row_permutation(32, True)
     assert perm[9] == 17 and perm[16 + 9] == 25 and perm[0] == 0 and perm[16] == 8
-    del nib
+    assert L.repacked_bytes(40, 80) == 4 * 2 * 576        # 40 rows pad to one 64-row group; 80 cols to 2 chunks
 
 
 # ------------------------------------------------------------------ shapes printed on the pages
