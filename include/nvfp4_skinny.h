@@ -52,10 +52,10 @@
 extern "C" {
 #endif
 
-#define NVFP4_LAYOUT_VERSION 1u
+#define NVFP4_LAYOUT_VERSION 2u
 
 /* Flags of an nvfp4_weight / nvfp4_repack call. */
-#define NVFP4_GATED 1u /* rows are [gate (N/2) || up (N/2)], N/2 % 8 == 0 */
+#define NVFP4_GATED 1u /* rows are [gate (N/2) || up (N/2)], N % 64 == 0 */
 
 typedef enum {
   NVFP4_OK = 0,
@@ -78,16 +78,19 @@ typedef enum {
  *                 must equal the flags given to nvfp4_repack().
  *   layout_version  NVFP4_LAYOUT_VERSION.
  *
- * Repacked layout (version 1): rows padded to a multiple of 16 and columns to a
- * multiple of 64 with zero bytes; a gated matrix first moves gate row i to row
- * 16*(i/8) + i%8 and up row i to 16*(i/8) + 8 + i%8.  The padded matrix is cut
- * into 576-byte tiles of 16 rows x 64 columns, row-block major.  In a tile,
- * byte 16*lane + 4*kt + r (lane = 4*g + t) holds columns c, c+1 of row
- * 16*rb + g + 8*(r&1) with c = 64*kc + 16*kt + 2*t + 8*(r>>1) (low nibble =
- * column c), and byte 512 + 8*g + 2*kt + h holds the scale of row
- * 16*rb + g + 8*h, group 4*kc + kt: one 16-byte load per lane gives an m16n8k16
- * A fragment for four 16-column groups.  Scale codes are stored with their sign
- * bit clear: a negative scale is folded into the signs of its 16 elements.
+ * Repacked layout (version 2): rows padded to a multiple of 64 and columns to a
+ * multiple of 64 with zero bytes; a gated matrix (n % 64 == 0) first moves gate
+ * row i to row 16*(i/8) + i%8 and up row i to 16*(i/8) + 8 + i%8.  The padded
+ * matrix is cut into 576-byte tiles of 16 rows x 64 columns; tile (64-row group
+ * G, 64-column chunk kc, 16-row block r) starts at byte 576*((G*KC + kc)*4 + r),
+ * KC = padded columns / 64, so the four tiles of one group and chunk are 2,304
+ * contiguous bytes.  In a tile, byte 16*lane + 4*kt + j (lane = 4*g + t) holds
+ * columns c, c+1 of the tile's row g + 8*(j&1) with c = 64*kc + 16*kt + 2*t +
+ * 8*(j>>1) (low nibble = column c), and byte 512 + 8*g + 2*kt + h holds the
+ * scale of the tile's row g + 8*h, group 4*kc + kt: one 16-byte load per lane
+ * gives an m16n8k16 A fragment for four 16-column groups.  Scale codes are
+ * stored with their sign bit clear: a negative scale is folded into the signs
+ * of its 16 elements.
  */
 typedef struct {
   const void *data;
@@ -138,7 +141,7 @@ nvfp4_status nvfp4_quantize(const float *w, int32_t num_matrices, int32_t n, int
  *   nibbles, scales (device) canonical, as written by nvfp4_quantize().
  *   out      (device) nvfp4_repacked_bytes(n, k, num_matrices) bytes, 16-byte
  *            aligned; every byte is written (padding with zeros).
- *   flags    0 or NVFP4_GATED (then n % 16 == 0).
+ *   flags    0 or NVFP4_GATED (then n % 64 == 0).
  */
 nvfp4_status nvfp4_repack(const uint8_t *nibbles, const uint8_t *scales, int32_t num_matrices, int32_t n,
                           int32_t k, uint32_t flags, void *out, cudaStream_t stream);

@@ -16,7 +16,7 @@ import torch
 from .build import LIB
 
 NVFP4_GATED = 1
-LAYOUT_VERSION = 1
+LAYOUT_VERSION = 2
 
 STATUS = {0: "ok", 1: "null pointer", 2: "bad shape", 3: "misaligned pointer",
           4: "workspace missing or too small", 5: "weight layout version or flags mismatch", 6: "CUDA error"}

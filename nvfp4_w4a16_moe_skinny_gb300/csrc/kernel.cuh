@@ -328,9 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const Job p) {
 #pragma unroll
           for (int i = 0; i < (kMMA ? 4 : 2); ++i)
             acc[a][b][i] *= mul[kMMA ? b * 8 + 2 * t4 + (i & 1) : b];
-      if (p.S == 1) {
+      if (kEpi == kEpiArgmax || p.S == 1) {  // the lm_head never splits K
         finish(grp, e);
-      } else {
+      } else if constexpr (kEpi != kEpiArgmax) {
         // ---- k-split: store the partial, take a ticket; the last slice sums all S in order
         const size_t gglob = static_cast<size_t>(seg) * p.ng + grp;
         float* mine = p.fix + ((gglob * p.S + s) * 32 + lane) * NACC;
@@ -359,20 +359,39 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const Job p) {
             for (int b = 0; b < B; ++b)
 #pragma unroll
               for (int i = 0; i < C; ++i) acc[a][b][i] = 0.f;
-          for (int ss = 0; ss < p.S; ++ss) {
-            const float* src = p.fix + ((gglob * p.S + ss) * 32 + lane) * NACC;
+          // slices in fixed order, up to kBatch slices' loads in flight at once
+          constexpr int kBatch = (kMMA && NT == 2) ? 1 : 2;  // registers: acc + kBatch slices
+          for (int s0 = 0; s0 < p.S; s0 += kBatch) {
+            constexpr int V = kMMA ? 4 : 2;
+            float buf[kBatch][4][B][V];
 #pragma unroll
-            for (int a = 0; a < 4; ++a)
+            for (int j = 0; j < kBatch; ++j) {
+              if (s0 + j < p.S) {
+                const float* src = p.fix + ((gglob * p.S + s0 + j) * 32 + lane) * NACC;
 #pragma unroll
-              for (int b = 0; b < B; ++b) {
-                const float* sp = src + (a * B + b) * C;
-                if constexpr (kMMA) {
-                  const float4 f = __ldcg(reinterpret_cast<const float4*>(sp));
-                  acc[a][b][0] += f.x, acc[a][b][1] += f.y, acc[a][b][2] += f.z, acc[a][b][3] += f.w;
-                } else {
-                  const float2 f = __ldcg(reinterpret_cast<const float2*>(sp));
-                  acc[a][b][0] += f.x, acc[a][b][1] += f.y;
-                }
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                  for (int b = 0; b < B; ++b) {
+                    const float* sp = src + (a * B + b) * C;
+                    if constexpr (kMMA) {
+                      const float4 f = __ldcg(reinterpret_cast<const float4*>(sp));
+                      buf[j][a][b][0] = f.x, buf[j][a][b][1] = f.y, buf[j][a][b][2 % V] = f.z, buf[j][a][b][3 % V] = f.w;
+                    } else {
+                      const float2 f = __ldcg(reinterpret_cast<const float2*>(sp));
+                      buf[j][a][b][0] = f.x, buf[j][a][b][1 % V] = f.y;
+                    }
+                  }
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+              if (s0 + j < p.S) {
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                  for (int b = 0; b < B; ++b)
+#pragma unroll
+                    for (int i = 0; i < C; ++i) acc[a][b][i] += buf[j][a][b][i];
               }
           }
           finish(grp, e);

@@ -37,16 +37,24 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   const int pairs = m * top_k;
   for (int t = warp; t < m; t += nwarps) {
     const float* row = logits + static_cast<size_t>(t) * n_experts;
+    // the lane's logits (experts lane + 32*i), read once
+    float lv[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = lane + 32 * i;
+      lv[i] = e < n_experts ? __ldg(row + e) : -INFINITY;
+    }
     uint32_t taken = 0;  // bit i: expert lane + 32*i already chosen (n_experts <= 1024)
     float chosen_v[32];
     int chosen_e[32];
     for (int r = 0; r < top_k; ++r) {
       float bv = -INFINITY;
       int be = 0x7FFFFFFF;
-      for (int i = 0; i * 32 < n_experts; ++i) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
         const int e = lane + 32 * i;
         if (e < n_experts && !((taken >> i) & 1u)) {
-          const float v = __ldg(row + e);
+          const float v = lv[i];
           if (v > bv || (v == bv && e < be)) bv = v, be = e;
         }
       }
@@ -116,11 +124,22 @@ __global__ void moe_combine_kernel(const float* __restrict__ d, const float* __r
   const size_t total = static_cast<size_t>(m) * cols;
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const int t = static_cast<int>(i / cols), j = static_cast<int>(i - static_cast<size_t>(t) * cols);
+    const int t = static_cast<int>(i / cols), j_col = static_cast<int>(i - static_cast<size_t>(t) * cols);
     float acc = 0.f;
-    for (int r = 0; r < top_k; ++r)
-      acc = fmaf(__ldg(probs + t * top_k + r), __ldg(d + static_cast<size_t>(t * top_k + r) * cols + j), acc);
-    if (shared) acc += __ldg(d + static_cast<size_t>(m * top_k + t) * cols + j);
+    // fixed slot order; the loads of 8 slots are issued before they are summed
+    for (int r0 = 0; r0 < top_k; r0 += 8) {
+      float pv[8], dv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = r0 + j;
+        pv[j] = r < top_k ? __ldg(probs + t * top_k + r) : 0.f;
+        dv[j] = r < top_k ? __ldg(d + static_cast<size_t>(t * top_k + r) * cols + j_col) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (r0 + j < top_k) acc = fmaf(pv[j], dv[j], acc);
+    }
+    if (shared) acc += __ldg(d + static_cast<size_t>(m * top_k + t) * cols + j_col);
     out[i] = f32_to_bf16_bits(acc);
   }
 }

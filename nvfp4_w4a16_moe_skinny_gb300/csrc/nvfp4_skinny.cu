@@ -72,7 +72,9 @@ int slots_of(int m) { return use_mma(m) ? (m <= 8 ? 8 : 16) : m; }
 int choose_split(long long pieces1, int kc, bool mma) {
   const long long warps = static_cast<long long>(kPlanSMs) * kWarps;
   if (pieces1 >= warps) return 1;
-  const int lmin = mma ? 4 : 2;  // shortest slice worth a fixup partial
+  // shortest slice worth a fixup partial: a partial costs a fence and 1-4 KiB
+  // through L2, against 2,304 B of weights per chunk
+  const int lmin = mma ? 8 : 4;
   int s = static_cast<int>((warps + pieces1 - 1) / pieces1);
   s = std::min(s, std::max(1, kc / lmin));
   s = std::min(s, kMaxSplit);

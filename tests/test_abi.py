@@ -44,7 +44,7 @@ def test_library_exports_every_declared_function(so):
 
 
 def test_status_strings_and_version(so):
-    assert so.nvfp4_layout_version() == 1
+    assert so.nvfp4_layout_version() == 2
     for code, text in [(0, b"ok"), (1, b"null pointer"), (2, b"bad shape"), (4, b"workspace missing or too small")]:
         assert so.nvfp4_status_string(code) == text
 
@@ -65,7 +65,7 @@ def test_sizes_reject_bad_shapes(so):
     assert so.moe_ffn_workspace_bytes(15, 8, 128, 2816, 704) >= (15 * 8 + 15) * (704 * 2 + 2816 * 4)
 
 
-def _weight(data=1 << 20, gs=1 << 20, n=64, k=64, e=1, flags=0, version=1):
+def _weight(data=1 << 20, gs=1 << 20, n=64, k=64, e=1, flags=0, version=2):
     from nvfp4_w4a16_moe_skinny_gb300.binding import CWeight
     return CWeight(data, gs, n, k, e, flags, version)
 
@@ -76,7 +76,7 @@ def test_gemm_argument_errors_return_before_any_launch(so):
     assert so.nvfp4_gemm(None, x, 1, y, ws, 1 << 20, None) == 1
     w = _weight(data=0)
     assert so.nvfp4_gemm(ctypes.byref(w), x, 1, y, ws, 1 << 20, None) == 1
-    w = _weight(version=2)
+    w = _weight(version=1)                            # weights repacked in the old tile order
     assert so.nvfp4_gemm(ctypes.byref(w), x, 1, y, ws, 1 << 20, None) == 5
     w = _weight(flags=1)
     assert so.nvfp4_gemm(ctypes.byref(w), x, 1, y, ws, 1 << 20, None) == 5
