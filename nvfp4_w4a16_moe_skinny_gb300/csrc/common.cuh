@@ -6,6 +6,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>  // CUtensorMap (the type only; the library does not link the driver API)
 #include <cuda_runtime.h>
 
 #include "nvfp4_skinny.h"
@@ -74,6 +75,23 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Bounded wait of one thread for the phase with the given parity to complete:
+// false, with kErrWaitTimeout recorded, if it did not within kWaitCycles.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait_sleep(bar, parity, 1u << 20)) {
+    if (clock64() - t0 > kWaitCycles) {
+      atomicOr(&g_device_error, kErrWaitTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
 // Bounded warp-collective wait (all 32 lanes call it) for the phase with the
 // given parity to complete.  Every lane observes the completion itself (so the
 // bulk-copied bytes are visible to it) and all lanes return the same answer:
@@ -108,6 +126,19 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// 4-D tiled tensor copy global -> shared (TMA engine) of the box at
+// coordinates (c0, c1, c2, c3) of `map`; completion is counted on `bar`.  The
+// destination is 128-byte aligned; c0 (the innermost coordinate) is 0 for every
+// copy of this library, so the 16-byte rule on it always holds.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // Four E2M1 pairs (the four bytes of w) -> four f16x2 (low nibble -> low half).
 __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
   asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
@@ -137,6 +168,29 @@ __device__ __forceinline__ uint32_t scale_lohi_x2(uint32_t w) {
   uint32_t r;
   asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(w), "n"(0x1404));  // bytes [0, s0, 0, s1]
   return r >> 1;
+}
+
+// Scale bytes J0 and J1 of `w` as an f16x2 (byte J0 -> low half, J1 -> high),
+// times 2^-8: PRMT places the two codes in bytes 1 and 3 of zeroed halves, then
+// a multiply by 128 (an integer multiply, off the ALU pipe) moves them to bits
+// 7..13 of each half.
+template <int J0, int J1>
+__device__ __forceinline__ uint32_t scale_pair_lohi(uint32_t w) {
+  constexpr uint32_t sel = (4 << 12) | (J1 << 8) | (4 << 4) | J0;  // bytes [sJ0, 0, sJ1, 0]
+  uint32_t r;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(w), "n"(sel));
+  uint32_t d;
+  asm("mul.lo.u32 %0, %1, 128;" : "=r"(d) : "r"(r));
+  return d;
+}
+
+// (a * [s.lo, s.lo], b * [s.hi, s.hi]): each half of `s` scales a whole f16x2.
+__device__ __forceinline__ void hmul2_bcast(uint32_t a, uint32_t b, uint32_t s, uint32_t& ra, uint32_t& rb) {
+  asm("{\n\t.reg .b16 l, h;\n\t.reg .b32 ll, hh;\n\t"
+      "mov.b32 {l, h}, %2;\n\tmov.b32 ll, {l, l};\n\tmov.b32 hh, {h, h};\n\t"
+      "mul.rn.f16x2 %0, %3, ll;\n\tmul.rn.f16x2 %1, %4, hh;\n\t}"
+      : "=r"(ra), "=r"(rb)
+      : "r"(s), "r"(a), "r"(b));
 }
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
@@ -182,6 +236,33 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], u
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+
+// Programmatic dependent launch.  wait: block until the grids this one depends
+// on have completed and their memory is visible (a no-op for a normal launch).
+// launch_dependents: let the next grid in the stream start its prologue.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
 __device__ __forceinline__ uint4 lds128(const void* p) {
   uint4 v;

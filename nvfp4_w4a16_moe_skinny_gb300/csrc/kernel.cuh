@@ -9,21 +9,37 @@
 //
 // Work decomposition.  A job is a list of *segments* (one matrix for the dense
 // GEMM and the lm_head; the experts that received tokens, then the shared
-// expert, for the MoE).  Each segment's matrix has `ng` 64-row groups and `kc`
-// 64-column chunks; K may be cut into S slices of L chunks.  The *pieces*
-// (segment, slice, group) are numbered segment-major, then slice, then group,
-// and dealt to the grid in contiguous, balanced ranges (one CTA of 16 warps per
-// SM).  A CTA walks its range in *runs* of one segment: it stages that
-// segment's tokens over the K columns the run touches (one barrier), and deals
-// the run's pieces to its warps round-robin.  A warp streams a piece's chunks
-// through its own ring, accumulating 4 tiles x tokens in registers.
+// expert, for the MoE).  Each segment's matrix has `ng` 64-row groups of four
+// 16-row tiles and `kc` 64-column chunks; K may be cut into S slices of L
+// chunks.  A *unit* is (segment, slice, group); units are numbered
+// segment-major, then slice, then group, and dealt to the grid in contiguous,
+// balanced ranges (one CTA of 16 warps per SM).  A CTA with at least 16 units
+// deals them whole, round-robin over its warps (the SM's issue slots, not the
+// warps, are then the limit, and whole units keep every copy four tiles wide);
+// a CTA with fewer deals their tiles as contiguous ranges, so every warp has
+// work.  A *piece* is one warp's share of one unit: 1 to 4 adjacent tiles over
+// the unit's K slice, streamed as TMA boxes of 4 tiles x 1 chunk, 3 x 1, 2 x 2
+// or 1 x 4.
 //
-// Epilogue.  S == 1: the piece holds the whole dot product and is finished in
-// registers.  S > 1: the warp stores its partial (already in output units) in
-// the fixup buffer and takes a ticket on the group's counter; the last of the S
-// slices to arrive sums the S partials in slice order and finishes the group.
-// No thread ever spins on another CTA.
+// Each CTA stages its activations once (the token rows over the columns its
+// units touch, or, for the down product, the gate+up outputs of its experts'
+// pairs), before any piece starts.
+//
+// Epilogue.  S == 1: the piece holds whole dot products and is finished in
+// registers.  S > 1: per tile, the warp stores its partial (already in output
+// units) in the fixup buffer and takes a ticket on the tile's counter; the
+// last of the S slices to arrive sums the S partials in slice order and
+// finishes the tile.  No thread ever spins on another CTA.
+//
+// Launch overlap.  Weights never depend on the previous kernel, so every warp
+// issues its first copies, then the CTA waits for the previous grid in the stream
+// (griddepcontrol.wait) before it reads activations, routing or workspace, and
+// only then lets the next grid start.  Outputs of the grid before the previous
+// one are therefore complete when a CTA starts: the down product reads the
+// routing before its wait.
 #pragma once
+
+#include <type_traits>
 
 #include "stream.cuh"
 
@@ -31,17 +47,20 @@ namespace nvfp4 {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
+constexpr int kMaxCtaSegs = 8;                 // segments whose units one CTA may hold
+constexpr int kMaxStagedRows = kMaxCtaSegs * 16;
 
 enum { kEpiStore = 0, kEpiArgmax = 1, kEpiGated = 2, kEpiRows = 3 };
 constexpr int kSharedSeg = -1;  // segment of the always-on shared expert
 constexpr int kDenseSeg = -2;   // the single segment of a dense job
 
+constexpr unsigned kErrPlan = 2u;  // a CTA's share exceeded the launch plan (g_device_error bit 1)
+
 struct Job {
-  const uint8_t* w;       // matrix 0 of the (stacked) weight
+  const uint8_t* w;       // the (stacked) weight: matrix e, group G, chunk c at ((e*ng + G)*kc + c)*2304
   const float* gs;        // global scales, one per matrix
   const uint8_t* w_sh;    // shared-expert matrix (MoE) or nullptr
-  const float* gs_sh;
-  size_t mat_bytes;       // repacked bytes of one matrix
+  const float* gs_sh;     // global scale of the shared expert (MoE) or nullptr
   int n, k;               // logical rows and columns of one matrix
   int ng, kc;             // 64-row groups, 64-column chunks
   int S, L;               // k-slices per group, chunks per slice
@@ -52,35 +71,34 @@ struct Job {
   const int* pairs;       // [m * top_k]
   int x_by_pair;          // MoE: 1 -> activation row = pair index (down); 0 -> token (gate_up)
   int has_shared;
+  int routing_ready;      // 1: the routing is complete before this grid starts (read before the wait)
   uint16_t* y;            // kEpiStore: y[tok * y_ld + row];  kEpiGated: h[pair * y_ld + i]
   int y_ld;
   float* yf;              // kEpiRows: d[pair * yf_ld + row]
   int yf_ld;
   float* fix;             // fixup partials (S > 1)
-  unsigned* fix_cnt;      // one counter per (segment, group)
+  unsigned* fix_cnt;      // one counter per (segment, group, tile)
   float* am_val;          // kEpiArgmax: per-CTA partial results [grid][m]
   int* am_idx;
   unsigned* am_cnt;
   float* max_logit;
   int* argmax;
   int ns;                 // ring stages per warp
-  int xs_chunks;          // capacity of the staged-activation buffer, in chunks
+  int xs_chunks;          // staged-activation capacity: chunks per row
+  int xs_rows;            // staged-activation capacity: rows (plus the zero row)
+  int max_cta_segs;       // segments one CTA may touch (<= kMaxCtaSegs)
 };
 
-template <int MT, bool kMMA>
-struct Acc {
-  static constexpr int NT = (MT + 7) / 8;
-  static constexpr int kPerLane = kMMA ? 4 * NT * 4 : 4 * MT * 2;
-};
+__host__ __device__ inline size_t stream_table_bytes(int n_experts) {
+  return static_cast<size_t>(4) * (kMaxStagedRows + (kMaxStagedRows + 1) + kMaxCtaSegs * 16 * 3 +
+                                   kWarps * 16 * 2 + kWarps * 8 + n_experts + 2 + 4);
+}
 
-__host__ __device__ inline size_t stream_smem_bytes(bool mma, int slots, int xs_chunks, int ns, int n_experts) {
-  const int nt = (slots + 7) / 8;
+__host__ __device__ inline size_t stream_smem_bytes(int xs_rows, int xs_chunks, int ns, int n_experts) {
   const size_t ring = static_cast<size_t>(kWarps) * ns * kStageBytes;
   const size_t bars = static_cast<size_t>(kWarps) * ns * 8;
-  const size_t xs = mma ? static_cast<size_t>(nt) * xs_chunks * kXFragChunkBytes
-                        : static_cast<size_t>(slots) * xs_chunks * kXCoreChunkBytes;
-  const size_t misc = 16 * 4 * 5 + kWarps * 16 * 8 + (static_cast<size_t>(n_experts) + 4) * 4 + 16;
-  return ring + bars + xs + misc;
+  const size_t xs = static_cast<size_t>(xs_rows + 1) * (static_cast<size_t>(xs_chunks) * kXChunkBytes + 16);
+  return ring + bars + xs + stream_table_bytes(n_experts);
 }
 
 __device__ __forceinline__ bool better(float v, int r, float bv, int br) {
@@ -94,32 +112,45 @@ __device__ __forceinline__ float gelu_tanh(float z) {
 }
 
 template <int MT, bool kMMA, int kEpi>
-__global__ void __launch_bounds__(kThreads, 1) stream_kernel(const Job p) {
-  constexpr int NT = Acc<MT, kMMA>::NT;
-  constexpr int SLOTS = kMMA ? NT * 8 : MT;
-  constexpr int NACC = Acc<MT, kMMA>::kPerLane;
+__global__ void __launch_bounds__(kThreads, 1)
+    stream_kernel(const __grid_constant__ Job p, const __grid_constant__ WeightMaps maps) {
+  constexpr int NT = (MT + 7) / 8;
+  constexpr int NA = kMMA ? NT : MT;   // accumulator columns per tile
+  constexpr int NI = kMMA ? 4 : 2;     // floats per accumulator column
+  constexpr int V = NA * NI;           // accumulator floats per lane and tile
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t4 = lane & 3;
 
-  // ---- shared memory carve-up
-  const size_t ring_bytes = static_cast<size_t>(kWarps) * p.ns * kStageBytes;
-  Ring ring{smem + static_cast<size_t>(warp) * p.ns * kStageBytes,
-            reinterpret_cast<uint64_t*>(smem + ring_bytes) + warp * p.ns, p.ns};
-  uint8_t* xs = smem + ring_bytes + static_cast<size_t>(kWarps) * p.ns * 8;
-  const size_t xs_bytes = kMMA ? static_cast<size_t>(NT) * p.xs_chunks * kXFragChunkBytes
-                               : static_cast<size_t>(SLOTS) * p.xs_chunks * kXCoreChunkBytes;
-  int* sigma = reinterpret_cast<int*>(xs + xs_bytes);
-  float* mul = reinterpret_cast<float*>(sigma + 16);
-  int* slot_row = reinterpret_cast<int*>(mul + 16);
-  int* slot_out = slot_row + 16;
-  unsigned* s_amax = reinterpret_cast<unsigned*>(slot_out + 16);
-  float* red_v = reinterpret_cast<float*>(s_amax + 16);
+  // ---- shared memory carve-up: warp w's stages at smem + w*ns*2304, then one
+  // mbarrier per stage, the staged activations and the tables
+  const int ns = p.ns;
+  const size_t ring_bytes = static_cast<size_t>(kWarps) * ns * kStageBytes;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + ring_bytes) + warp * ns;  // this warp's barriers
+  uint8_t* xs = smem + ring_bytes + static_cast<size_t>(kWarps) * ns * 8;
+  const size_t xs_bytes = static_cast<size_t>(p.xs_rows + 1) * (static_cast<size_t>(p.xs_chunks) * kXChunkBytes + 16);
+  int* row_src = reinterpret_cast<int*>(xs + xs_bytes);                      // [kMaxStagedRows]
+  int* sigma = row_src + kMaxStagedRows;                                     // [kMaxStagedRows + 1]
+  int* slot_row = sigma + kMaxStagedRows + 1;                                // [kMaxCtaSegs * 16]
+  int* slot_out = slot_row + kMaxCtaSegs * 16;
+  float* mul = reinterpret_cast<float*>(slot_out + kMaxCtaSegs * 16);
+  float* red_v = mul + kMaxCtaSegs * 16;                                     // [kWarps * 16]
   int* red_i = reinterpret_cast<int*>(red_v + kWarps * 16);
-  int* seg_list = red_i + kWarps * 16;   // [n_experts + 1]
-  int* misc = seg_list + p.n_experts + 2;  // [0] = segment count, [1] = last-arrival flag
+  int* cur = red_i + kWarps * 16 + warp * 8;                                 // [kWarps * 8] copy cursors
+  int* seg_list = red_i + kWarps * 16 + kWarps * 8;                          // [n_experts + 2]
+  int* misc = seg_list + p.n_experts + 2;  // [0] segments, [1] last-arrival flag, [2] staged rows
 
-  // ---- segments
-  if (p.n_experts == 0) {
+  if (lane == 0) {
+    for (int s = 0; s < ns; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  // ---- segments: the dense matrix, or the experts that received pairs, then the shared expert
+  const bool dense = p.n_experts == 0;
+  const bool early = dense || p.routing_ready;
+  if (!early) pdl_wait();
+  if (dense) {
     if (threadIdx.x == 0) seg_list[0] = kDenseSeg, misc[0] = 1;
   } else if (warp == 0) {
     int n = 0;
@@ -137,274 +168,357 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const Job p) {
   }
   __syncthreads();
   const int n_seg = misc[0];
-  const int per_seg = p.S * p.ng;  // pieces per segment
-  const long long n_pieces = static_cast<long long>(n_seg) * per_seg;
-  const int p0 = static_cast<int>(n_pieces * blockIdx.x / gridDim.x);
-  const int p1 = static_cast<int>(n_pieces * (blockIdx.x + 1) / gridDim.x);
+  const int per_seg = p.S * p.ng;  // units per segment
+  const long long n_units = static_cast<long long>(n_seg) * per_seg;
+  const int u0 = static_cast<int>(n_units * blockIdx.x / gridDim.x);
+  const int u1 = static_cast<int>(n_units * (blockIdx.x + 1) / gridDim.x);
+  int nu = u1 - u0;
+  // this CTA's segments and K columns (chunks [c_lo, c_hi))
+  const int cseg0 = nu > 0 ? u0 / per_seg : 0;
+  const int nsc = nu > 0 ? (u1 - 1) / per_seg - cseg0 + 1 : 0;
+  int c_lo = 0, c_hi = nu > 0 ? p.kc : 0;
+  if (nsc == 1) {
+    c_lo = ((u0 - cseg0 * per_seg) / p.ng) * p.L;
+    c_hi = min(p.kc, ((u1 - 1 - cseg0 * per_seg) / p.ng + 1) * p.L);
+  }
+  if (nsc > p.max_cta_segs || c_hi - c_lo > p.xs_chunks || (smem_addr(smem) & 127u)) {
+    // the launch plan does not cover this CTA's share: record it and do no work
+    if (threadIdx.x == 0) atomicOr(&g_device_error, kErrPlan);
+    nu = 0;
+  }
+  const int nsc_used = nu > 0 ? nsc : 0;
+  if (nu == 0) c_lo = c_hi = 0;  // nothing to stage
 
-  // runs: consecutive pieces of one segment
-  const int seg0 = per_seg ? p0 / per_seg : 0;
-  const int n_runs = (p1 > p0) ? (p1 - 1) / per_seg - seg0 + 1 : 0;
-  auto run_lo = [&](int r) { return max(p0, (seg0 + r) * per_seg); };
-  auto run_hi = [&](int r) { return min(p1, (seg0 + r + 1) * per_seg); };
-  auto run_units = [&](int r) {
-    const int len = run_hi(r) - run_lo(r);
-    return len > warp ? (len - warp + kWarps - 1) / kWarps : 0;
+  // ---- warp w's pieces: with at least 16 units, whole units round-robin (warp w
+  // takes units w, w+16, ...); with fewer, the units' tiles as contiguous ranges
+  const bool whole = nu >= kWarps;
+  struct Piece {
+    int seg, s, grp, t0, tn;
   };
-  auto matrix_of = [&](int seg) -> const uint8_t* {
-    const int e = seg_list[seg];
-    if (e == kSharedSeg) return p.w_sh;
-    if (e == kDenseSeg) return p.w;
-    return p.w + static_cast<size_t>(e) * p.mat_bytes;
+  const int T0 = (4 * nu * warp) / kWarps, T1 = (4 * nu * (warp + 1)) / kWarps;
+  const int n_pieces = whole ? (nu - warp + kWarps - 1) / kWarps
+                             : (T1 > T0 ? ((T1 - 1) >> 2) - (T0 >> 2) + 1 : 0);
+  auto piece_at = [&](int k) -> Piece {
+    int unit, t0, tn;
+    if (whole) {
+      unit = u0 + k * kWarps + warp, t0 = 0, tn = 4;
+    } else {
+      const int start = k == 0 ? T0 : ((T0 >> 2) + k) << 2;
+      const int end = min(T1, ((T0 >> 2) + k + 1) << 2);
+      unit = u0 + (start >> 2), t0 = start & 3, tn = end - start;
+    }
+    Piece pc;
+    pc.seg = unit / per_seg;
+    const int r = unit - pc.seg * per_seg;
+    pc.s = r / p.ng;
+    pc.grp = r - pc.s * p.ng;
+    pc.t0 = t0, pc.tn = tn;
+    return pc;
   };
-  // piece -> (slice, group); chunks of slice s are [s*L, min(kc, (s+1)*L))
-  auto slice_of = [&](int piece, int seg) { return (piece - seg * per_seg) / p.ng; };
-  auto group_of = [&](int piece, int seg) { return (piece - seg * per_seg) % p.ng; };
   auto slice_len = [&](int s) { return min(p.kc, (s + 1) * p.L) - s * p.L; };
 
-  // ---- producer (lane 0): cursor over this warp's pieces; chunk addresses are
-  // recomputed only at piece boundaries (a piece's chunks are contiguous)
-  int pr = 0, pu = 0;             // run, unit of the next piece to open
-  const uint8_t* pptr = nullptr;  // next chunk to copy
-  int prem = 0;                   // chunks left in the open piece
+  // ---- producer (lane 0): cursor over this warp's pieces.  A piece of tn tiles
+  // is ceil(chunks / copy_chunks(tn)) copies; the last may run past the slice
+  // (those chunks are loaded, or zero-filled past K, and not used).  The cursor
+  // lives in shared memory (lane 0's only), not in registers: [0] next piece,
+  // [1] copies left, [2] map index (tn-1, +4 for the shared expert), [3] t0,
+  // [4] next chunk, [5] group, [6] chunks per copy.
+  if (lane == 0) cur[0] = 0, cur[1] = 0;
   const uint64_t policy = l2_evict_first_policy();
+  uint8_t* ring = smem + static_cast<size_t>(warp) * ns * kStageBytes;
   auto issue_next = [&](int stage) {
-    if (prem == 0) {
-      while (pr < n_runs && pu >= run_units(pr)) pu = 0, ++pr;
-      if (pr >= n_runs) return;
-      const int seg = seg0 + pr;
-      const int piece = run_lo(pr) + warp + pu * kWarps;
-      const int sl = slice_of(piece, seg), grp = group_of(piece, seg);
-      pptr = matrix_of(seg) + (static_cast<size_t>(grp) * p.kc + sl * p.L) * kStageBytes;
-      prem = slice_len(sl);
-      ++pu;
+    if (cur[1] == 0) {
+      if (cur[0] >= n_pieces) return;
+      const Piece pc = piece_at(cur[0]++);
+      const int e = seg_list[pc.seg];
+      const int step = copy_chunks(pc.tn);
+      cur[1] = (slice_len(pc.s) + step - 1) / step;
+      cur[2] = (pc.tn - 1) + (e == kSharedSeg ? 4 : 0);
+      cur[3] = pc.t0;
+      cur[4] = pc.s * p.L;
+      cur[5] = (e >= 0 ? e * p.ng : 0) + pc.grp;
+      cur[6] = step;
     }
-    ring_issue(ring, stage, pptr, policy);
-    pptr += kStageBytes;
-    --prem;
+    const int mi = cur[2];
+    const uint32_t bytes = static_cast<uint32_t>(((mi & 3) + 1) * cur[6]) * kTileBytes;
+    mbar_arrive_expect_tx(&bar[stage], bytes);
+    if ((mi & 3) == 3) {
+      // four tiles of one chunk are 2,304 contiguous bytes: a plain bulk copy
+      const uint8_t* base = mi < 4 ? p.w : p.w_sh;
+      bulk_g2s(ring + stage * kStageBytes,
+               base + (static_cast<size_t>(cur[5]) * p.kc + cur[4]) * kStageBytes, kStageBytes, &bar[stage], policy);
+    } else {
+      const CUtensorMap* map = mi < 4 ? &maps.w[mi] : &maps.sh[mi - 4];
+      tma_load_4d(ring + stage * kStageBytes, map, 0, cur[3], cur[4], cur[5], &bar[stage], policy);
+    }
+    cur[4] += cur[6];
+    --cur[1];
   };
-  ring_init(ring, lane);
   if (lane == 0)
-    for (int st = 0; st < p.ns; ++st) issue_next(st);
+    for (int st = 0; st < ns; ++st) issue_next(st);
 
-  const int g = lane >> 2, t4 = lane & 3;
+  if (early) pdl_wait();
+  pdl_launch_dependents();
+
+  // ---- staged rows and the (segment, slot) tables
+  const int stride = (c_hi - c_lo) * kXChunkBytes + 16;
+  if (threadIdx.x == 0) {
+    int nrows = 0;
+    if (!p.x_by_pair) {
+      nrows = nsc_used ? p.m : 0;
+      for (int j = 0; j < nrows; ++j) row_src[j] = j;
+    } else {
+      for (int i = 0; i < nsc_used; ++i) {
+        const int e = seg_list[cseg0 + i];
+        if (e == kSharedSeg) {
+          for (int j = 0; j < p.m; ++j) row_src[nrows++] = p.m * p.top_k + j;
+        } else {
+          const int o = __ldg(p.offsets + e), cnt = min(p.m, __ldg(p.offsets + e + 1) - o);
+          for (int j = 0; j < cnt; ++j) row_src[nrows++] = __ldg(p.pairs + o + j);
+        }
+      }
+    }
+    misc[2] = nrows;
+  }
+  __syncthreads();
+  const int nrows = misc[2];
+  if (threadIdx.x < nsc_used * 16) {
+    const int i = threadIdx.x >> 4, j = threadIdx.x & 15;
+    const int e = seg_list[cseg0 + i];
+    int row = nrows, out = -1;  // empty slot: the zero row, no output
+    if (e == kDenseSeg) {
+      if (j < p.m) row = out = j;
+    } else {
+      // first staged row of segment i (down product: rows are per segment)
+      int base = 0;
+      if (p.x_by_pair)
+        for (int ii = 0; ii < i; ++ii) {
+          const int ee = seg_list[cseg0 + ii];
+          base += ee == kSharedSeg ? p.m : min(p.m, __ldg(p.offsets + ee + 1) - __ldg(p.offsets + ee));
+        }
+      if (e == kSharedSeg) {
+        if (j < p.m) out = p.m * p.top_k + j, row = p.x_by_pair ? base + j : j;
+      } else {
+        const int o = __ldg(p.offsets + e), cnt = min(p.m, __ldg(p.offsets + e + 1) - o);
+        if (j < cnt) {
+          out = __ldg(p.pairs + o + j);
+          row = p.x_by_pair ? base + j : out / p.top_k;
+        }
+      }
+    }
+    slot_row[threadIdx.x] = row;
+    slot_out[threadIdx.x] = out;
+  }
+  stage_rows<kMMA>(p.x, p.k, c_lo * kTileK, c_hi - c_lo, nrows, row_src, sigma, xs, stride);
+  if (threadIdx.x < nsc_used * 16) {
+    const int e = seg_list[cseg0 + (threadIdx.x >> 4)];
+    const float gsc = (e == kSharedSeg) ? __ldg(p.gs_sh) : (e == kDenseSeg ? __ldg(p.gs) : __ldg(p.gs + e));
+    const int row = slot_row[threadIdx.x];
+    mul[threadIdx.x] = row < nrows ? gsc * exp2i(8 - sigma[row]) : 0.f;
+  }
+  __syncthreads();
+
   const CoreLane cl(lane);
-  float acc[kMMA ? 4 : 4][kMMA ? NT : MT][kMMA ? 4 : 2];
+  const uint32_t xs_addr = smem_addr(xs);
+  float acc[4][NA][NI];
   constexpr int NBEST = kMMA ? NT * 2 : MT;
   float bv[NBEST];
   int bi[NBEST];
 #pragma unroll
   for (int i = 0; i < NBEST; ++i) bv[i] = -INFINITY, bi[i] = 0x7FFFFFFF;
 
-  // Finish a group whose full dot products are in `acc` (output units, i.e. already
-  // multiplied by mul).  grp = 64-row group within the segment.
-  auto finish = [&](int grp, int e) {
-    if constexpr (!kMMA) {
-      // CUDA-core partials are per 16-column group q: sum over the 4 lanes of a row pair
+  // Finish tile t (0..3) of group grp of local segment sl from a[] (output units).
+  auto finish_tile = [&](int sl, int grp, int t, const float (&a)[NA][NI]) {
+    const int rb = grp * 4 + t;  // 16-row block within the matrix
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+    for (int c = 0; c < NA; ++c)
 #pragma unroll
-        for (int mm = 0; mm < MT; ++mm)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float v = acc[r][mm][h];
-            v += __shfl_xor_sync(0xffffffffu, v, 1);
-            v += __shfl_xor_sync(0xffffffffu, v, 2);
-            acc[r][mm][h] = v;
+      for (int i = 0; i < NI; ++i) {
+        const int hrow = kMMA ? (i >> 1) : i;  // 0: row g, 1: row g+8
+        const int slot = kMMA ? c * 8 + 2 * t4 + (i & 1) : c;
+        const float v = a[c][i];
+        const int row = rb * 16 + g + 8 * hrow;
+        if constexpr (kEpi == kEpiStore) {
+          if ((kMMA || t4 == 0) && slot < p.m && row < p.n) p.y[static_cast<size_t>(slot) * p.y_ld + row] = f32_to_bf16_bits(v);
+        } else if constexpr (kEpi == kEpiRows) {
+          const int out = slot_out[sl * 16 + slot];
+          if ((kMMA || t4 == 0) && out >= 0 && row < p.n) p.yf[static_cast<size_t>(out) * p.yf_ld + row] = v;
+        } else if constexpr (kEpi == kEpiArgmax) {
+          const int b = kMMA ? c * 2 + (i & 1) : c;
+          if (row < p.n && better(v, row, bv[b], bi[b])) bv[b] = v, bi[b] = row;
+        } else {  // kEpiGated: rows g = gate i, g+8 = up i of block rb, i = rb*8 + g
+          if (hrow == 0) {
+            const float up = a[c][kMMA ? i + 2 : 1];
+            const int out = slot_out[sl * 16 + slot];
+            if ((kMMA || t4 == 0) && out >= 0)
+              p.y[static_cast<size_t>(out) * p.y_ld + rb * 8 + g] = f32_to_bf16_bits(gelu_tanh(v) * up);
           }
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int rb = grp * 4 + r;  // 16-row block within the matrix
-#pragma unroll
-      for (int a = 0; a < (kMMA ? NT : MT); ++a)
-#pragma unroll
-        for (int i = 0; i < (kMMA ? 4 : 2); ++i) {
-          const int hrow = kMMA ? (i >> 1) : i;                        // 0: row g, 1: row g+8
-          const int slot = kMMA ? a * 8 + 2 * t4 + (i & 1) : a;
-          const float v = acc[r][a][i];
-          if constexpr (kEpi == kEpiStore) {
-            const int row = rb * 16 + g + 8 * hrow;
-            if ((kMMA || t4 == 0) && slot < p.m && row < p.n)
-              p.y[static_cast<size_t>(slot) * p.y_ld + row] = f32_to_bf16_bits(v);
-          } else if constexpr (kEpi == kEpiRows) {
-            const int row = rb * 16 + g + 8 * hrow;
-            const int out = slot_out[slot];
-            if ((kMMA || t4 == 0) && out >= 0 && row < p.n) p.yf[static_cast<size_t>(out) * p.yf_ld + row] = v;
-          } else if constexpr (kEpi == kEpiArgmax) {
-            const int row = rb * 16 + g + 8 * hrow;
-            const int b = kMMA ? a * 2 + (i & 1) : a;
-            if (row < p.n && better(v, row, bv[b], bi[b])) bv[b] = v, bi[b] = row;
-          } else {  // kEpiGated: rows g = gate i, g+8 = up i of block rb, i = rb*8 + g
-            if (hrow == 0) {
-              const float gate = v, up = acc[r][a][kMMA ? i + 2 : 1];
-              const int out = slot_out[slot];
-              if ((kMMA || t4 == 0) && out >= 0)
-                p.y[static_cast<size_t>(out) * p.y_ld + rb * 8 + g] = f32_to_bf16_bits(gelu_tanh(gate) * up);
-            }
-          }
-        }
-    }
-    (void)e;
-  };
-
-  int st = 0;            // ring stage of the next chunk
-  uint32_t ph = 0;       // its mbarrier parity
-  bool failed = false;   // a copy did not complete in time
-  // every warp runs every iteration of this loop (its barriers are CTA-wide); a
-  // warp whose copy timed out only skips its own chunks
-  for (int r = 0; r < n_runs; ++r) {
-    const int seg = seg0 + r;
-    const int e = seg_list[seg];
-    const int lo = run_lo(r), hi = run_hi(r);
-    const int s_lo = slice_of(lo, seg), s_hi = slice_of(hi - 1, seg);
-    const int kc_lo = s_lo * p.L, kc_hi = min(p.kc, (s_hi + 1) * p.L);
-    // ---- stage this run's tokens over columns [64 kc_lo, 64 kc_hi)
-    __syncthreads();
-    if (threadIdx.x < 16) {
-      const int j = threadIdx.x;
-      int row = -1, out = -1;
-      if (e == kDenseSeg) {
-        if (j < p.m) row = out = j;
-      } else if (e == kSharedSeg) {
-        if (j < p.m) out = p.m * p.top_k + j, row = p.x_by_pair ? out : j;
-      } else {
-        const int o = __ldg(p.offsets + e), cnt = __ldg(p.offsets + e + 1) - o;
-        if (j < cnt) {
-          out = __ldg(p.pairs + o + j);
-          row = p.x_by_pair ? out : out / p.top_k;
         }
       }
-      slot_row[j] = j < SLOTS ? row : -1;
-      slot_out[j] = j < SLOTS ? out : -1;
-    }
-    __syncthreads();
-    auto tok_row = [&](int slot) -> int { return slot_row[slot]; };
-    stage_tokens<kMMA, SLOTS>(p.x, p.k, kc_lo * kTileK, kc_hi - kc_lo, tok_row, s_amax, sigma, xs);
-    if (threadIdx.x < SLOTS) {
-      const float gsc = (e == kSharedSeg) ? __ldg(p.gs_sh) : (e == kDenseSeg ? __ldg(p.gs) : __ldg(p.gs + e));
-      mul[threadIdx.x] = gsc * exp2i(8 - sigma[threadIdx.x]);
-    }
-    __syncthreads();
+  };
 
-    const int units = run_units(r);
-    for (int u = 0; u < units && !failed; ++u) {
-      const int piece = lo + warp + u * kWarps;
-      const int s = slice_of(piece, seg), grp = group_of(piece, seg);
-      const int nch = slice_len(s);
+
+  {
+    // ---- stream the pieces through the ring
+    const uint32_t ring_addr = smem_addr(ring);
+    int st = 0;           // ring stage of the next copy
+    uint32_t ph = 0;      // its mbarrier parity
+    bool failed = false;  // a copy did not complete in time
+    for (int k = 0; k < n_pieces && !failed; ++k) {
+      const Piece pc = piece_at(k);
+      const int sl = pc.seg - cseg0;
+      const int kc0 = pc.s * p.L, nch = slice_len(pc.s);
+      const uint32_t xbase = xs_addr + (kc0 - c_lo) * kXChunkBytes;
+      uint32_t xr[NA];
+#pragma unroll
+      for (int c = 0; c < NA; ++c) {
+        if constexpr (kMMA)
+          xr[c] = xbase + slot_row[sl * 16 + c * 8 + g] * stride + t4 * 32;
+        else
+          xr[c] = xbase + slot_row[sl * 16 + c] * stride;
+      }
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < (kMMA ? NT : MT); ++b)
+        for (int c = 0; c < NA; ++c)
 #pragma unroll
-          for (int i = 0; i < (kMMA ? 4 : 2); ++i) acc[a][b][i] = 0.f;
-      const uint8_t* xchunk = xs + static_cast<size_t>(s * p.L - kc_lo) * (kMMA ? NT * kXFragChunkBytes : MT * kXCoreChunkBytes);
-      for (int c = 0; c < nch; ++c) {
-        if (!mbar_wait_warp(&ring.bar[st], ph)) {
+          for (int i = 0; i < NI; ++i) acc[a][c][i] = 0.f;
+      const int step = copy_chunks(pc.tn);
+      for (int ch = 0; ch < nch; ch += step) {
+        if (!mbar_wait_warp(&bar[st], ph)) {
           failed = true;
           break;
         }
-        const uint8_t* stage = ring.buf + st * kStageBytes;
-        if constexpr (kMMA) {
-          mma_chunk<NT>(stage, xchunk, lane, acc);
-          xchunk += NT * kXFragChunkBytes;
-        } else {
-          core_chunk<MT>(stage, xchunk, cl, acc);
-          xchunk += MT * kXCoreChunkBytes;
+        const uint32_t stage = ring_addr + st * kStageBytes;
+        const int cnt = min(step, nch - ch);  // chunks of this copy inside the slice
+        // the copy's chunks, each TN tiles at stage + cc*TN*576
+        auto consume = [&](auto tn_c) {
+          constexpr int TN = decltype(tn_c)::value;
+          for (int cc = 0; cc < cnt; ++cc) {
+            const uint32_t sub = stage + cc * TN * kTileBytes;
+            if constexpr (kMMA)
+              mma_chunk<NT, TN>(sub, xr, lane, acc);
+            else
+              core_chunk<MT, TN>(sub, xr, cl, acc);
+#pragma unroll
+            for (int c = 0; c < NA; ++c) xr[c] += kXChunkBytes;
+          }
+        };
+        switch (pc.tn) {
+          case 4: consume(std::integral_constant<int, 4>{}); break;
+          case 3: consume(std::integral_constant<int, 3>{}); break;
+          case 2: consume(std::integral_constant<int, 2>{}); break;
+          default: consume(std::integral_constant<int, 1>{}); break;
         }
         __syncwarp();
         if (lane == 0) {
-          fence_proxy_async_smem();
+          fence_proxy_async_smem();  // this warp's reads of the stage before the next copy into it
           issue_next(st);
         }
-        if (++st == p.ns) st = 0, ph ^= 1u;
+        if (++st == ns) st = 0, ph ^= 1u;
       }
       if (failed) break;
-      // ---- to output units
+      // ---- to output units (CUDA cores: first the sum over the 4 lanes of a row pair)
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < 4; ++a) {
+        if (a >= pc.tn) break;
 #pragma unroll
-        for (int b = 0; b < (kMMA ? NT : MT); ++b)
+        for (int c = 0; c < NA; ++c)
 #pragma unroll
-          for (int i = 0; i < (kMMA ? 4 : 2); ++i)
-            acc[a][b][i] *= mul[kMMA ? b * 8 + 2 * t4 + (i & 1) : b];
+          for (int i = 0; i < NI; ++i) {
+            float v = acc[a][c][i];
+            if constexpr (!kMMA) {
+              v += __shfl_xor_sync(0xffffffffu, v, 1);
+              v += __shfl_xor_sync(0xffffffffu, v, 2);
+            }
+            acc[a][c][i] = v * mul[sl * 16 + (kMMA ? c * 8 + 2 * t4 + (i & 1) : c)];
+          }
+      }
       if (kEpi == kEpiArgmax || p.S == 1) {  // the lm_head never splits K
-        finish(grp, e);
-      } else if constexpr (kEpi != kEpiArgmax) {
-        // ---- k-split: store the partial, take a ticket; the last slice sums all S in order
-        const size_t gglob = static_cast<size_t>(seg) * p.ng + grp;
-        float* mine = p.fix + ((gglob * p.S + s) * 32 + lane) * NACC;
-        constexpr int B = kMMA ? NT : MT, C = kMMA ? 4 : 2;
 #pragma unroll
         for (int a = 0; a < 4; ++a)
+          if (a < pc.tn) finish_tile(sl, pc.grp, pc.t0 + a, acc[a]);
+      } else if constexpr (kEpi != kEpiArgmax) {
+        // ---- k-split: per tile, store the partial and take a ticket; the last of
+        // the S slices sums all S partials in slice order and finishes the tile
+        const size_t cell0 = (static_cast<size_t>(pc.seg) * p.ng + pc.grp) * 4 + pc.t0;
 #pragma unroll
-          for (int b = 0; b < B; ++b) {
-            float* dst = mine + (a * B + b) * C;
+        for (int a = 0; a < 4; ++a) {
+          if (a >= pc.tn) break;
+          float* dst = p.fix + (((cell0 + a) * p.S + pc.s) * 32 + lane) * V;
+#pragma unroll
+          for (int c = 0; c < NA; ++c) {
             if constexpr (kMMA)
-              __stcg(reinterpret_cast<float4*>(dst), make_float4(acc[a][b][0], acc[a][b][1], acc[a][b][2], acc[a][b][3]));
+              __stcg(reinterpret_cast<float4*>(dst + c * 4), make_float4(acc[a][c][0], acc[a][c][1], acc[a][c][2], acc[a][c][3]));
             else
-              __stcg(reinterpret_cast<float2*>(dst), make_float2(acc[a][b][0], acc[a][b][1]));
+              __stcg(reinterpret_cast<float2*>(dst + c * 2), make_float2(acc[a][c][0], acc[a][c][1]));
           }
+        }
         __threadfence();
         __syncwarp();
-        unsigned ticket = 0;
-        if (lane == 0) ticket = atomicAdd(&p.fix_cnt[gglob], 1u);
-        ticket = __shfl_sync(0xffffffffu, ticket, 0);
-        if (ticket == static_cast<unsigned>(p.S - 1)) {
-          if (lane == 0) atomicExch(&p.fix_cnt[gglob], 0u);
-          __threadfence();
+        unsigned last = 0;  // bit a: this warp completed tile t0 + a
+        if (lane == 0) {
+          unsigned tk[4];
 #pragma unroll
           for (int a = 0; a < 4; ++a)
+            if (a < pc.tn) tk[a] = atomicAdd(&p.fix_cnt[cell0 + a], 1u);
 #pragma unroll
-            for (int b = 0; b < B; ++b)
+          for (int a = 0; a < 4; ++a)
+            if (a < pc.tn && tk[a] == static_cast<unsigned>(p.S - 1)) {
+              last |= 1u << a;
+              atomicExch(&p.fix_cnt[cell0 + a], 0u);
+            }
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) __threadfence();
 #pragma unroll
-              for (int i = 0; i < C; ++i) acc[a][b][i] = 0.f;
-          // slices in fixed order, up to kBatch slices' loads in flight at once
-          constexpr int kBatch = (kMMA && NT == 2) ? 1 : 2;  // registers: acc + kBatch slices
+        for (int a = 0; a < 4; ++a) {
+          if (!((last >> a) & 1u)) continue;
+          float sum[NA][NI];
+#pragma unroll
+          for (int c = 0; c < NA; ++c)
+#pragma unroll
+            for (int i = 0; i < NI; ++i) sum[c][i] = 0.f;
+          const float* src0 = p.fix + ((cell0 + a) * p.S * 32 + lane) * V;
+          constexpr int kBatch = V >= 12 ? 1 : (V >= 8 ? 2 : 4);  // slices in flight together (registers)
           for (int s0 = 0; s0 < p.S; s0 += kBatch) {
-            constexpr int V = kMMA ? 4 : 2;
-            float buf[kBatch][4][B][V];
+            float buf[kBatch][NA][NI];
 #pragma unroll
             for (int j = 0; j < kBatch; ++j) {
               if (s0 + j < p.S) {
-                const float* src = p.fix + ((gglob * p.S + s0 + j) * 32 + lane) * NACC;
+                const float* src = src0 + static_cast<size_t>(s0 + j) * 32 * V;
 #pragma unroll
-                for (int a = 0; a < 4; ++a)
-#pragma unroll
-                  for (int b = 0; b < B; ++b) {
-                    const float* sp = src + (a * B + b) * C;
-                    if constexpr (kMMA) {
-                      const float4 f = __ldcg(reinterpret_cast<const float4*>(sp));
-                      buf[j][a][b][0] = f.x, buf[j][a][b][1] = f.y, buf[j][a][b][2 % V] = f.z, buf[j][a][b][3 % V] = f.w;
-                    } else {
-                      const float2 f = __ldcg(reinterpret_cast<const float2*>(sp));
-                      buf[j][a][b][0] = f.x, buf[j][a][b][1 % V] = f.y;
-                    }
+                for (int c = 0; c < NA; ++c) {
+                  if constexpr (kMMA) {
+                    const float4 f = __ldcg(reinterpret_cast<const float4*>(src + c * 4));
+                    buf[j][c][0] = f.x, buf[j][c][1] = f.y, buf[j][c][2 % NI] = f.z, buf[j][c][3 % NI] = f.w;
+                  } else {
+                    const float2 f = __ldcg(reinterpret_cast<const float2*>(src + c * 2));
+                    buf[j][c][0] = f.x, buf[j][c][1 % NI] = f.y;
                   }
+                }
               }
             }
 #pragma unroll
             for (int j = 0; j < kBatch; ++j)
               if (s0 + j < p.S) {
 #pragma unroll
-                for (int a = 0; a < 4; ++a)
+                for (int c = 0; c < NA; ++c)
 #pragma unroll
-                  for (int b = 0; b < B; ++b)
-#pragma unroll
-                    for (int i = 0; i < C; ++i) acc[a][b][i] += buf[j][a][b][i];
+                  for (int i = 0; i < NI; ++i) sum[c][i] += buf[j][c][i];
               }
           }
-          finish(grp, e);
+          finish_tile(sl, pc.grp, pc.t0 + a, sum);
         }
       }
     }
-  }
-  if (failed) {
-    // a copy did not complete in time: wait (bounded) for the copies this warp
-    // may still have in flight so none lands after the CTA exits, then give up
-    for (int i = 1; i < p.ns; ++i) {
-      if (++st == p.ns) st = 0, ph ^= 1u;
-      (void)mbar_wait_warp(&ring.bar[st], ph);
+    if (failed) {
+      // a copy did not complete in time: wait (bounded) for the copies this warp
+      // may still have in flight so none lands after the CTA exits, then give up
+      for (int i = 1; i < ns; ++i) {
+        if (++st == ns) st = 0, ph ^= 1u;
+        (void)mbar_wait_warp(&bar[st], ph);
+      }
     }
   }
 

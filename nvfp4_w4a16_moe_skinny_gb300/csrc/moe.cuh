@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   const int pairs = m * top_k;
+  pdl_wait();  // the logits may come from the previous grid
+  pdl_launch_dependents();
   for (int t = warp; t < m; t += nwarps) {
     const float* row = logits + static_cast<size_t>(t) * n_experts;
     // the lane's logits (experts lane + 32*i), read once
@@ -121,6 +123,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 // out[t, j] = bf16( sum_r probs[t, r] * d[t*top_k + r, j] + d[m*top_k + t, j] ), fixed order.
 __global__ void moe_combine_kernel(const float* __restrict__ d, const float* __restrict__ probs, int m, int top_k,
                                    int cols, bool shared, uint16_t* __restrict__ out) {
+  pdl_wait();  // d comes from the previous grid
+  pdl_launch_dependents();
   const size_t total = static_cast<size_t>(m) * cols;
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {

@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -55,89 +56,213 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 // ------------------------------------------------------------------ streaming-kernel plans
 // The K split S is chosen from the shapes alone, against a fixed reference
 // parallelism (152 SMs x 16 warps), so workspace sizes are host-computable and
-// identical on every device; the grid is the device's SM count.
+// identical on every device; the grid is the device's SM count, and the staging
+// capacities are sized for that grid.
 constexpr int kPlanSMs = 152;
 constexpr int kMaxSplit = 16;
 
 struct Plan {
-  int S, L, ns, xs_chunks;
+  int S, L, ns, xs_chunks, xs_rows, max_cta_segs, grid;
   size_t smem;
 };
 
-int nacc_per_lane(int m) { return m <= 7 ? 4 * m * 2 : (m <= 8 ? 16 : 32); }
 bool use_mma(int m) { return m >= 8; }
-int slots_of(int m) { return use_mma(m) ? (m <= 8 ? 8 : 16) : m; }
+// accumulator floats per lane and 16-row tile (the fixup partial of one tile)
+int acc_per_tile(int m) { return use_mma(m) ? (m <= 8 ? 4 : 8) : 2 * m; }
 
-// S for `pieces1` (segments x groups) unsplit pieces of kc chunks each.
-int choose_split(long long pieces1, int kc, bool mma) {
-  const long long warps = static_cast<long long>(kPlanSMs) * kWarps;
-  if (pieces1 >= warps) return 1;
-  // shortest slice worth a fixup partial: a partial costs a fence and 1-4 KiB
-  // through L2, against 2,304 B of weights per chunk
-  const int lmin = mma ? 8 : 4;
-  int s = static_cast<int>((warps + pieces1 - 1) / pieces1);
-  s = std::min(s, std::max(1, kc / lmin));
-  s = std::min(s, kMaxSplit);
-  const int L = ceil_div(kc, s);
-  return ceil_div(kc, L);
+// A fixup area is a fixed 256 KiB of arrival counters (one per segment x group x
+// tile, at most 65,536) followed by the partials.  The counters sit at the same
+// place whatever the shape, and every call leaves them zero, so one zero-filled
+// workspace can serve calls of different shapes.
+constexpr size_t kFixCounterBytes = 256 * 1024;
+
+size_t fixup_bytes(int m, int S, int ng, int n_seg_max) {
+  if (S <= 1) return 0;
+  return kFixCounterBytes + static_cast<size_t>(n_seg_max) * ng * 4 * S * 32 * acc_per_tile(m) * sizeof(float);
 }
 
-bool make_plan(int m, int S, int ng, int kc, int n_seg_max, int n_experts, Plan* out) {
-  const int sms = std::max(1, sm_count());
-  const bool mma = use_mma(m);
-  const int slots = slots_of(m);
+// Launch plan for split S on a grid of multiples of `sms` CTAs: one CTA per SM
+// (more, in waves, if a CTA would otherwise hold units of more than kMaxCtaSegs
+// segments -- only on devices with few SMs), staging capacities that cover the
+// busiest CTA, then the deepest ring that fits in shared memory.
+bool make_plan(int m, int S, int ng, int kc, int n_seg_max, int n_experts, bool x_by_pair, int sms, Plan* out) {
   const int L = ceil_div(kc, S);
-  int xs_chunks = kc;
-  if (S > 1) {
-    const long long pc = (static_cast<long long>(n_seg_max) * S * ng + sms - 1) / sms;
-    xs_chunks = static_cast<int>(std::min<long long>(kc, ((pc + ng - 1) / ng + 1) * L));
+  const int per_seg = S * ng;
+  int grid = sms;
+  long long nu_max = 0;
+  int segs = 0;
+  for (;; grid += sms) {
+    nu_max = (static_cast<long long>(n_seg_max) * per_seg + grid - 1) / grid;
+    segs = static_cast<int>(std::min<long long>(n_seg_max, (nu_max + per_seg - 1) / per_seg + 1));
+    if (segs <= kMaxCtaSegs) break;
   }
+  int xs_chunks = kc;
+  if (segs == 1) xs_chunks = static_cast<int>(std::min<long long>(kc, ((nu_max + ng - 1) / ng + 1) * L));
+  const int xs_rows = x_by_pair ? segs * m : m;
   for (int ns = 8; ns >= 2; --ns) {
-    const size_t smem = stream_smem_bytes(mma, slots, xs_chunks, ns, n_experts);
+    const size_t smem = stream_smem_bytes(xs_rows, xs_chunks, ns, n_experts);
     if (smem <= kMaxSmem) {
-      *out = Plan{S, L, ns, xs_chunks, smem};
+      *out = Plan{S, L, ns, xs_chunks, xs_rows, segs, grid, smem};
       return true;
     }
   }
   return false;
 }
 
+// Predicted time (us) of one launch of `plan` over n_seg segments of ng groups,
+// on the reference grid: staging the activations, then the slowest of the
+// busiest SM's share of HBM, its dequantisation throughput and its busiest
+// warp's chain of copies (at most ns in flight), plus the fixup when K is
+// split.  Only used to rank the splits.
+double plan_cost(int m, int ng, int n_seg, bool x_by_pair, const Plan& plan) {
+  const int S = plan.S, L = plan.L;
+  const long long units = static_cast<long long>(n_seg) * S * ng;
+  const long long nu = (units + kPlanSMs - 1) / kPlanSMs;  // units of the busiest CTA
+  // copies in the busiest warp's chain: whole units round-robin, or (fewer than
+  // 16 units) at most two pieces of its tile range, 1, 2 or 4 chunks per copy
+  long long chain;
+  if (nu >= kWarps) {
+    chain = (nu + kWarps - 1) / kWarps * L;
+  } else {
+    const int tiles = static_cast<int>(std::max<long long>(1, (4 * nu + kWarps - 1) / kWarps));
+    chain = tiles >= 3 ? 2 * L : (L + copy_chunks(tiles) - 1) / copy_chunks(tiles);
+  }
+  const int rows = x_by_pair ? m * std::min(plan.max_cta_segs, 2) : m;
+  const double t_stage = 1.0 + static_cast<double>(rows) * plan.xs_chunks * kXChunkBytes / 20000.0;
+  const double tiles_per_us = use_mma(m) ? 65.0 : (m <= 2 ? 90.0 : 220.0 / (m + 1));
+  const double copy_us = std::max(0.22, 1.3 / plan.ns);  // one warp's copies, ns in flight
+  const double t_mem = static_cast<double>(nu) * L * kStageBytes / 40000.0;  // 40 GB/s per SM
+  const double t_alu = static_cast<double>(nu) * 4 * L / tiles_per_us;
+  const double t_lat = static_cast<double>(chain) * copy_us;
+  // fixup: a fence and a ticket, then the last slice reads the S partials a few at a time
+  const int v = acc_per_tile(m), batch = v >= 12 ? 1 : (v >= 8 ? 2 : 4);
+  const double t_fix = S > 1 ? 1.2 + 0.35 * ((S + batch - 1) / batch) : 0.0;
+  return t_stage + std::max(t_mem, std::max(t_alu, t_lat)) + t_fix;
+}
+
+// S for a job: the cheapest by plan_cost (ties to the smaller S), planned on the
+// reference grid so that it depends on the shapes only.  n_seg_est is the
+// expected number of segments, n_seg_max the most there can be.
+int choose_split(int m, int ng, int kc, int n_seg_est, int n_seg_max, int n_experts, bool x_by_pair,
+                 bool allow_split) {
+  int best = 1;
+  double best_cost = 1e30;
+  Plan pl;
+  if (make_plan(m, 1, ng, kc, n_seg_max, n_experts, x_by_pair, kPlanSMs, &pl))
+    best_cost = plan_cost(m, ng, n_seg_est, x_by_pair, pl);
+  if (!allow_split) return 1;
+  if (static_cast<size_t>(n_seg_max) * ng * 4 > kFixCounterBytes / sizeof(unsigned)) return 1;
+  for (int s = 2; s <= std::min(kMaxSplit, kc); ++s) {
+    const int L = ceil_div(kc, s);
+    if (ceil_div(kc, L) != s) continue;  // the same slices as a smaller S
+    if (!make_plan(m, s, ng, kc, n_seg_max, n_experts, x_by_pair, kPlanSMs, &pl)) continue;
+    const double c = plan_cost(m, ng, n_seg_est, x_by_pair, pl);
+    if (c < best_cost * 0.97) best = s, best_cost = c;
+  }
+  return best;
+}
+
+// ------------------------------------------------------------------ TMA tensor maps
+// cuTensorMapEncodeTiled is a driver-API function; the library reaches it through
+// the runtime's entry-point query, so it links only the runtime.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// The four tensor maps (boxes of 1..4 tiles, see WeightMaps) of the repacked
+// weight stack `w`: num_matrices x ceil(n/64) groups of ceil(k/64) chunks.
+bool encode_weight_maps(const nvfp4_weight* w, CUtensorMap (&maps)[4]) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const int kc = ceil_div(w->k, kTileK);
+  const cuuint64_t groups = static_cast<cuuint64_t>(w->num_matrices) * ceil_div(w->n, kGroupRows);
+  const cuuint64_t dims[4] = {kTileBytes / 8, kChunkTiles, static_cast<cuuint64_t>(kc), groups};
+  const cuuint64_t strides[3] = {kTileBytes, kStageBytes, static_cast<cuuint64_t>(kc) * kStageBytes};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  for (int tn = 1; tn <= 4; ++tn) {
+    const cuuint32_t box[4] = {kTileBytes / 8, static_cast<cuuint32_t>(tn), static_cast<cuuint32_t>(copy_chunks(tn)), 1};
+    if (fn(&maps[tn - 1], CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, const_cast<void*>(w->data), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
+// Maps of a weight and, for a MoE layer, of its shared expert.
+bool make_maps(const nvfp4_weight* w, const nvfp4_weight* shared, WeightMaps* out) {
+  if (!encode_weight_maps(w, out->w)) return false;
+  if (shared) return encode_weight_maps(shared, out->sh);
+  for (int i = 0; i < 4; ++i) out->sh[i] = out->w[i];
+  return true;
+}
+
+// Programmatic dependent launch (see kernel.cuh, "Launch overlap"); switched off
+// by NVFP4_PDL=0 in the environment, for comparison runs.
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("NVFP4_PDL");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <int MT, bool kMMA, int kEpi>
-nvfp4_status launch_stream(Job p, const Plan& plan, cudaStream_t stream) {
+nvfp4_status launch_stream(Job p, const WeightMaps& maps, const Plan& plan, cudaStream_t stream) {
   auto kernel = stream_kernel<MT, kMMA, kEpi>;
   if (set_smem(kernel, plan.smem) != cudaSuccess) return NVFP4_ERR_CUDA;
   p.S = plan.S;
   p.L = plan.L;
   p.ns = plan.ns;
   p.xs_chunks = plan.xs_chunks;
-  kernel<<<std::max(1, sm_count()), kThreads, plan.smem, stream>>>(p);
+  p.xs_rows = plan.xs_rows;
+  p.max_cta_segs = plan.max_cta_segs;
+  if (launch_pdl(kernel, dim3(plan.grid), dim3(kThreads), plan.smem, stream, p, maps) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
   return launched();
 }
 
 template <int kEpi>
-nvfp4_status dispatch_stream(const Job& p, const Plan& plan, cudaStream_t stream) {
+nvfp4_status dispatch_stream(const Job& p, const WeightMaps& maps, const Plan& plan, cudaStream_t stream) {
   switch (p.m) {
-    case 1: return launch_stream<1, false, kEpi>(p, plan, stream);
-    case 2: return launch_stream<2, false, kEpi>(p, plan, stream);
-    case 3: return launch_stream<3, false, kEpi>(p, plan, stream);
-    case 4: return launch_stream<4, false, kEpi>(p, plan, stream);
-    case 5: return launch_stream<5, false, kEpi>(p, plan, stream);
-    case 6: return launch_stream<6, false, kEpi>(p, plan, stream);
-    case 7: return launch_stream<7, false, kEpi>(p, plan, stream);
-    case 8: return launch_stream<8, true, kEpi>(p, plan, stream);
-    default: return launch_stream<16, true, kEpi>(p, plan, stream);
+    case 1: return launch_stream<1, false, kEpi>(p, maps, plan, stream);
+    case 2: return launch_stream<2, false, kEpi>(p, maps, plan, stream);
+    case 3: return launch_stream<3, false, kEpi>(p, maps, plan, stream);
+    case 4: return launch_stream<4, false, kEpi>(p, maps, plan, stream);
+    case 5: return launch_stream<5, false, kEpi>(p, maps, plan, stream);
+    case 6: return launch_stream<6, false, kEpi>(p, maps, plan, stream);
+    case 7: return launch_stream<7, false, kEpi>(p, maps, plan, stream);
+    case 8: return launch_stream<8, true, kEpi>(p, maps, plan, stream);
+    default: return launch_stream<16, true, kEpi>(p, maps, plan, stream);
   }
-}
-
-// A fixup area is a fixed 64 KiB of arrival counters (one per segment x group,
-// at most 16,384) followed by the partials.  The counters sit at the same place
-// whatever the shape, and every call leaves them zero, so one zero-filled
-// workspace can serve calls of different shapes.
-constexpr size_t kFixCounterBytes = 64 * 1024;
-
-size_t fixup_bytes(int m, int S, int ng, int n_seg_max) {
-  if (S <= 1) return 0;
-  return kFixCounterBytes + static_cast<size_t>(n_seg_max) * ng * S * 32 * nacc_per_lane(m) * sizeof(float);
 }
 
 void set_fixup(Job* p, void* base) {
@@ -157,7 +282,7 @@ Job dense_job(const nvfp4_weight* w, const uint16_t* x, int m) {
 }
 
 int dense_split(int m, int n, int k) {
-  return choose_split(ceil_div(n, kGroupRows), ceil_div(k, kTileK), use_mma(m));
+  return choose_split(m, ceil_div(n, kGroupRows), ceil_div(k, kTileK), 1, 1, 0, false, true);
 }
 
 }  // namespace
@@ -258,8 +383,10 @@ nvfp4_status nvfp4_gemm(const nvfp4_weight* w, const uint16_t* x, int32_t m, uin
   p.y_ld = w->n;
   set_fixup(&p, ws);
   Plan plan;
-  if (!make_plan(m, dense_split(m, w->n, w->k), p.ng, p.kc, 1, 0, &plan)) return NVFP4_ERR_SHAPE;
-  return dispatch_stream<kEpiStore>(p, plan, stream);
+  if (!make_plan(m, dense_split(m, w->n, w->k), p.ng, p.kc, 1, 0, false, std::max(1, sm_count()), &plan)) return NVFP4_ERR_SHAPE;
+  WeightMaps maps;
+  if (!make_maps(w, nullptr, &maps)) return NVFP4_ERR_CUDA;
+  return dispatch_stream<kEpiStore>(p, maps, plan, stream);
 }
 
 size_t lm_head_workspace_bytes(int32_t m, int32_t vocab) {
@@ -282,8 +409,10 @@ nvfp4_status lm_head_launch(const nvfp4_weight* w, const uint16_t* x, int32_t m,
   p.max_logit = max_logit;
   p.argmax = argmax;
   Plan plan;
-  if (!make_plan(m, 1, p.ng, p.kc, 1, 0, &plan)) return NVFP4_ERR_SHAPE;
-  return dispatch_stream<kEpiArgmax>(p, plan, stream);
+  if (!make_plan(m, 1, p.ng, p.kc, 1, 0, false, std::max(1, sm_count()), &plan)) return NVFP4_ERR_SHAPE;
+  WeightMaps maps;
+  if (!make_maps(w, nullptr, &maps)) return NVFP4_ERR_CUDA;
+  return dispatch_stream<kEpiArgmax>(p, maps, plan, stream);
 }
 
 }  // namespace
@@ -327,11 +456,11 @@ struct MoESplits {
 MoESplits moe_splits(int m, int top_k, int n_experts, int d, int inter, bool shared) {
   const int n_seg_est = expected_segments(m, top_k, n_experts, shared);
   MoESplits r;
-  r.s_gu = choose_split(static_cast<long long>(n_seg_est) * ceil_div(2 * inter, kGroupRows), ceil_div(d, kTileK),
-                        use_mma(m));
-  r.s_dn = choose_split(static_cast<long long>(n_seg_est) * ceil_div(d, kGroupRows), ceil_div(inter, kTileK),
-                        use_mma(m));
   r.n_seg_max = std::min(n_experts, m * top_k) + (shared ? 1 : 0);
+  r.s_gu = choose_split(m, ceil_div(2 * inter, kGroupRows), ceil_div(d, kTileK), n_seg_est, r.n_seg_max, n_experts,
+                        false, true);
+  r.s_dn = choose_split(m, ceil_div(d, kGroupRows), ceil_div(inter, kTileK), n_seg_est, r.n_seg_max, n_experts,
+                        true, true);
   return r;
 }
 
@@ -368,8 +497,9 @@ nvfp4_status moe_route_topk(const float* logits, int32_t m, int32_t n_experts, i
     return NVFP4_ERR_ALIGN;
   const size_t smem = sizeof(int) * (static_cast<size_t>(m) * top_k + n_experts + 1);
   if (set_smem(moe_route_kernel, smem) != cudaSuccess) return NVFP4_ERR_CUDA;
-  moe_route_kernel<<<1, kRouteThreads, smem, stream>>>(logits, m, n_experts, top_k, ids, probs, expert_offsets,
-                                                        sorted_pairs);
+  if (launch_pdl(moe_route_kernel, dim3(1), dim3(kRouteThreads), smem, stream, logits, m, n_experts, top_k, ids, probs,
+                 expert_offsets, sorted_pairs) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
   return launched();
 }
 
@@ -413,7 +543,6 @@ nvfp4_status moe_ffn_grouped(const uint16_t* x, int32_t m, int32_t top_k, const 
   a.gs = gate_up->global_scale;
   a.w_sh = shared ? static_cast<const uint8_t*>(shared_gate_up->data) : nullptr;
   a.gs_sh = shared ? shared_gate_up->global_scale : nullptr;
-  a.mat_bytes = nvfp4_repacked_bytes(2 * inter, d, 1);
   a.n = 2 * inter, a.k = d;
   a.ng = ceil_div(2 * inter, kGroupRows), a.kc = ceil_div(d, kTileK);
   a.x = x;
@@ -424,29 +553,35 @@ nvfp4_status moe_ffn_grouped(const uint16_t* x, int32_t m, int32_t top_k, const 
   a.y = h, a.y_ld = inter;
   set_fixup(&a, base + wl.h + wl.d);
   Plan pa;
-  if (!make_plan(m, sp.s_gu, a.ng, a.kc, sp.n_seg_max, n_exp, &pa)) return NVFP4_ERR_SHAPE;
-  if (const nvfp4_status st = dispatch_stream<kEpiGated>(a, pa, stream)) return st;
+  if (!make_plan(m, sp.s_gu, a.ng, a.kc, sp.n_seg_max, n_exp, false, std::max(1, sm_count()), &pa)) return NVFP4_ERR_SHAPE;
+  WeightMaps ma;
+  if (!make_maps(gate_up, shared ? shared_gate_up : nullptr, &ma)) return NVFP4_ERR_CUDA;
+  if (const nvfp4_status st = dispatch_stream<kEpiGated>(a, ma, pa, stream)) return st;
 
   Job b = a;
   b.w = static_cast<const uint8_t*>(down->data);
   b.gs = down->global_scale;
   b.w_sh = shared ? static_cast<const uint8_t*>(shared_down->data) : nullptr;
   b.gs_sh = shared ? shared_down->global_scale : nullptr;
-  b.mat_bytes = nvfp4_repacked_bytes(d, inter, 1);
   b.n = d, b.k = inter;
   b.ng = ceil_div(d, kGroupRows), b.kc = ceil_div(inter, kTileK);
   b.x = h;
   b.x_by_pair = 1;
+  b.routing_ready = 1;  // the gate+up grid before it waited for the routing
   b.y = nullptr;
   b.yf = dpart, b.yf_ld = d;
   set_fixup(&b, base + wl.h + wl.d);
   Plan pb;
-  if (!make_plan(m, sp.s_dn, b.ng, b.kc, sp.n_seg_max, n_exp, &pb)) return NVFP4_ERR_SHAPE;
-  if (const nvfp4_status st = dispatch_stream<kEpiRows>(b, pb, stream)) return st;
+  if (!make_plan(m, sp.s_dn, b.ng, b.kc, sp.n_seg_max, n_exp, true, std::max(1, sm_count()), &pb)) return NVFP4_ERR_SHAPE;
+  WeightMaps mb;
+  if (!make_maps(down, shared ? shared_down : nullptr, &mb)) return NVFP4_ERR_CUDA;
+  if (const nvfp4_status st = dispatch_stream<kEpiRows>(b, mb, pb, stream)) return st;
 
   const size_t total = static_cast<size_t>(m) * d;
   const int blocks = static_cast<int>(std::min<size_t>((total + 255) / 256, static_cast<size_t>(sm_count()) * 4));
-  moe_combine_kernel<<<std::max(1, blocks), 256, 0, stream>>>(dpart, probs, m, top_k, d, shared, out);
+  if (launch_pdl(moe_combine_kernel, dim3(std::max(1, blocks)), dim3(256), 0, stream, static_cast<const float*>(dpart),
+                 probs, m, top_k, d, shared, out) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
   return launched();
 }
 

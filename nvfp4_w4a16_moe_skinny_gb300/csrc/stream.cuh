@@ -1,27 +1,33 @@
-// Per-warp weight streaming and the chunk consumers (sm_103a).
+// Per-warp weight streaming, the chunk consumers and activation staging (sm_103a).
 //
-// A *chunk* is the four 576-byte tiles of one 64-row group and one 64-column
-// slice of K (2,304 contiguous bytes in the repacked layout, version 2).  Every
-// warp owns a private ring of `ns` chunk-sized stages in shared memory.  Lane 0
-// fills a stage with one 1-D bulk copy (TMA engine, L2 evict-first); the whole
-// warp waits on the stage's mbarrier; when the warp has consumed a stage, lane 0
-// refills it with the chunk `ns` positions ahead.  No stage is shared between
+// A *chunk* is the tiles of one 64-row group and one 64-column slice of K (four
+// 576-byte tiles, 2,304 contiguous bytes in the repacked layout, version 2).  A
+// warp streams 1 to 4 adjacent tiles of a group through its private ring of
+// `ns` 2,304-byte stages in shared memory.  Lane 0 fills a stage with one tiled
+// tensor copy (TMA engine, L2 evict-first) of those tiles over 1, 2 or 4
+// consecutive chunks (4 tiles x 1, 3 x 1, 2 x 2 or 1 x 4 chunks); the whole warp
+// waits on the stage's mbarrier; when the warp has consumed a stage, lane 0
+// refills it with the copy `ns` positions ahead.  No stage is shared between
 // warps, so the only synchronisation is the mbarrier (copy -> warp) and
 // __syncwarp (warp -> refill).
 //
+// Activations are staged once per CTA as f16 rows (each row rescaled by a power
+// of two), 128 bytes per row and 64-column chunk, one warp per row.  A consumer
+// reaches the rows of its token slots through per-lane row addresses, so one
+// staged copy of the tokens serves every expert of a grouped product.
+//
 // Chunk consumers:
-//  * mma_chunk<NT>: tensor cores (m16n8k16, f16 in, f32 accumulate); each tile's
-//    16 rows are the A operand and up to 8*NT tokens the N operand.  The x
-//    fragments of the 64 columns are loaded once and feed the four tiles, which
-//    also gives four independent accumulator chains.  Each E2M1 pair goes
-//    through the hardware converter and is multiplied in f16 by its E4M3 scale
-//    (exact: the product has at most 6 significant bits).
-//  * core_chunk<MT>: CUDA cores for up to 7 tokens.  Lane (g, q) takes rows g and
-//    g+8 of each tile over the 16-column group q; it sums E2M1 x activation
-//    products in f32 (mixed-precision FMA; the products are exact) and scales
-//    each group sum once (MT <= 2), or scales the weights in f16 first and
-//    accumulates directly (MT >= 3, fewer live registers).  The cross-lane sum
-//    over q is left to warp shuffles in the epilogue.
+//  * mma_chunk<NT, TN>: tensor cores (m16n8k16, f16 in, f32 accumulate); each
+//    tile's 16 rows are the A operand and up to 8*NT token slots the N operand.
+//    The x fragments of the 64 columns are loaded once and feed the TN tiles.
+//    Each E2M1 pair goes through the hardware converter and is multiplied in f16
+//    by its E4M3 scale (exact: the product has at most 6 significant bits).
+//  * core_chunk<MT, TN>: CUDA cores for up to 7 tokens.  Lane (g, q) takes rows
+//    g and g+8 of each tile over the 16-column group q; it sums E2M1 x
+//    activation products in f32 (mixed-precision FMA; the products are exact)
+//    and scales each group sum once (MT <= 2), or scales the weights in f16
+//    first and accumulates directly (MT >= 3, fewer live registers).  The
+//    cross-lane sum over q is left to warp shuffles in the epilogue.
 #pragma once
 
 #include "common.cuh"
@@ -30,42 +36,40 @@ namespace nvfp4 {
 
 constexpr int kChunkTiles = 4;                          // tiles per chunk (one 64-row group)
 constexpr int kStageBytes = kChunkTiles * kTileBytes;   // 2,304 bytes
-
-// x fragments for the MMA path, per 64-column chunk and 8-token group: 32 lanes x
-// 8 words (f16x2).  Lane (g, t), word 2*kt + h holds token slot g, columns
-// 16*kt + 2*t + 8*h (+1) of the chunk -- the m16n8k16 B fragment.
-constexpr int kXFragChunkBytes = 1024;
-// x for the CUDA-core path, per 64-column chunk and token: 32 f16x2 words (pairs).
-constexpr int kXCoreChunkBytes = 128;
+// Staged activations: bytes per row and 64-column chunk (32 f16 pairs).  MMA
+// order: lane (g, t) reads 32 contiguous bytes at 32*t, word 2*kt + h holding
+// columns 16*kt + 2*t + 8*h (+1) -- the m16n8k16 B fragment of token slot g.
+// CUDA-core order: pair j (columns 2j, 2j+1) at word j.
+constexpr int kXChunkBytes = 128;
 
 template <int NT>
-__device__ __forceinline__ void mma_step(uint32_t word, uint32_t sg, uint32_t sg8, const uint32_t (&b0)[NT],
+__device__ __forceinline__ void mma_step(uint32_t word, uint32_t s, const uint32_t (&b0)[NT],
                                          const uint32_t (&b1)[NT], float (&acc)[NT][4]) {
   uint32_t h[4];
   e2m1x8_to_f16x2(word, h);
   uint32_t a[4];
-  a[0] = hmul2(h[0], sg);   // row g,   columns 2t, 2t+1
-  a[1] = hmul2(h[1], sg8);  // row g+8, columns 2t, 2t+1
-  a[2] = hmul2(h[2], sg);   // row g,   columns 2t+8, 2t+9
-  a[3] = hmul2(h[3], sg8);  // row g+8, columns 2t+8, 2t+9
+  hmul2_bcast(h[0], h[1], s, a[0], a[1]);  // rows g, g+8, columns 2t, 2t+1
+  hmul2_bcast(h[2], h[3], s, a[2], a[3]);  // rows g, g+8, columns 2t+8, 2t+9
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) mma_f16(acc[nt], a, b0[nt], b1[nt]);
 }
 
-// One chunk (4 tiles at `st`) against x fragments `xf` (NT * 1024 bytes).
-// acc[r][nt] is tile r's C fragment: [0],[1] = row g, tokens 8nt+2t, +1; [2],[3] = row g+8.
-template <int NT>
-__device__ __forceinline__ void mma_chunk(const uint8_t* st, const uint8_t* xf, int lane, float (&acc)[4][NT][4]) {
+// TN tiles at shared address `st` against x fragments at xr[nt] (this lane's 32
+// bytes of slot 8*nt + g for the chunk).  acc[r][nt] is tile r's C fragment:
+// [0],[1] = row g, slots 8nt+2t, +1; [2],[3] = row g+8.
+template <int NT, int TN>
+__device__ __forceinline__ void mma_chunk(uint32_t st, const uint32_t (&xr)[NT], int lane,
+                                          float (&acc)[4][NT][4]) {
   uint4 xa[NT], xb[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    xa[nt] = lds128(xf + nt * kXFragChunkBytes + lane * 32);
-    xb[nt] = lds128(xf + nt * kXFragChunkBytes + lane * 32 + 16);
+    xa[nt] = lds128(xr[nt]);
+    xb[nt] = lds128(xr[nt] + 16);
   }
-  uint4 wv[4];
-  uint2 sv[4];
+  uint4 wv[TN];
+  uint2 sv[TN];
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
+  for (int r = 0; r < TN; ++r) {
     wv[r] = lds128(st + r * kTileBytes + lane * 16);
     sv[r] = lds64(st + r * kTileBytes + kTileNibBytes + (lane >> 2) * 8);
   }
@@ -73,34 +77,28 @@ __device__ __forceinline__ void mma_chunk(const uint8_t* st, const uint8_t* xf, 
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) b0[nt] = xa[nt].x, b1[nt] = xa[nt].y;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) mma_step<NT>(wv[r].x, scale_pair_x2<0>(sv[r].x), scale_pair_x2<1>(sv[r].x), b0, b1, acc[r]);
+  for (int r = 0; r < TN; ++r) mma_step<NT>(wv[r].x, scale_pair_lohi<0, 1>(sv[r].x), b0, b1, acc[r]);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) b0[nt] = xa[nt].z, b1[nt] = xa[nt].w;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) mma_step<NT>(wv[r].y, scale_pair_x2<2>(sv[r].x), scale_pair_x2<3>(sv[r].x), b0, b1, acc[r]);
+  for (int r = 0; r < TN; ++r) mma_step<NT>(wv[r].y, scale_pair_lohi<2, 3>(sv[r].x), b0, b1, acc[r]);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) b0[nt] = xb[nt].x, b1[nt] = xb[nt].y;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) mma_step<NT>(wv[r].z, scale_pair_x2<0>(sv[r].y), scale_pair_x2<1>(sv[r].y), b0, b1, acc[r]);
+  for (int r = 0; r < TN; ++r) mma_step<NT>(wv[r].z, scale_pair_lohi<0, 1>(sv[r].y), b0, b1, acc[r]);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) b0[nt] = xb[nt].z, b1[nt] = xb[nt].w;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) mma_step<NT>(wv[r].w, scale_pair_x2<2>(sv[r].y), scale_pair_x2<3>(sv[r].y), b0, b1, acc[r]);
-}
-
-__device__ __forceinline__ uint32_t lds_u16(const void* p) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(smem_addr(p)));
-  return v;
+  for (int r = 0; r < TN; ++r) mma_step<NT>(wv[r].w, scale_pair_lohi<2, 3>(sv[r].y), b0, b1, acc[r]);
 }
 
 // Per-lane constants of the CUDA-core consumer: lane (g, q) reads, at step j, the
 // 32-bit word q of lane-chunk t_j = (j + g/2) & 3 of row pair g (the rotation by
 // g/2 puts the 32 lanes on 32 distinct banks) and the x pairs 8q + t_j, 8q + t_j + 4.
 struct CoreLane {
-  int w_off[4];   // byte offset of the weight word within a tile
-  int x_off[4];   // byte offset of x pair 8q + t_j within a token's 64-column chunk
-  int s_off;      // byte offset of the scale pair (rows g, g+8; group q) within a tile
+  uint32_t w_off[4];  // byte offset of the weight word within a tile
+  uint32_t x_off[4];  // byte offset of x pair 8q + t_j within a row's 64-column chunk
+  uint32_t s_off;     // byte offset of the scale pair (rows g, g+8; group q) within a tile
   __device__ __forceinline__ CoreLane(int lane) {
     const int g = lane >> 2, q = lane & 3;
 #pragma unroll
@@ -113,24 +111,24 @@ struct CoreLane {
   }
 };
 
-// One chunk on CUDA cores.  xw: the chunk's x words [MT][32 words].  acc[r][m][0]
-// = tile r, row g; acc[r][m][1] = row g+8 (partial over this lane's group q).
-template <int MT>
-__device__ __forceinline__ void core_chunk(const uint8_t* st, const uint8_t* xw, const CoreLane& cl,
+// TN tiles at `st` on CUDA cores.  xr[m]: token m's staged row for this chunk.
+// acc[r][m][0] = tile r, row g; acc[r][m][1] = row g+8 (partial over group q).
+template <int MT, int TN>
+__device__ __forceinline__ void core_chunk(uint32_t st, const uint32_t (&xr)[MT], const CoreLane& cl,
                                            float (&acc)[4][MT][2]) {
   if constexpr (MT <= 2) {
-    uint32_t xr[MT][4][2];
+    uint32_t xw[MT][4][2];
 #pragma unroll
     for (int m = 0; m < MT; ++m)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        xr[m][j][0] = lds32(xw + m * kXCoreChunkBytes + cl.x_off[j]);
-        xr[m][j][1] = lds32(xw + m * kXCoreChunkBytes + cl.x_off[j] + 16);
+        xw[m][j][0] = lds32(xr[m] + cl.x_off[j]);
+        xw[m][j][1] = lds32(xr[m] + cl.x_off[j] + 16);
       }
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const uint8_t* tile = st + r * kTileBytes;
-      const uint32_t sp = scale_lohi_x2(lds_u16(tile + cl.s_off));
+    for (int r = 0; r < TN; ++r) {
+      const uint32_t tile = st + r * kTileBytes;
+      const uint32_t sp = scale_pair_lohi<0, 1>(lds16(tile + cl.s_off));
       float pa[MT], pb[MT], pc[MT], pd[MT];
 #pragma unroll
       for (int m = 0; m < MT; ++m) pa[m] = pb[m] = pc[m] = pd[m] = 0.f;
@@ -140,14 +138,14 @@ __device__ __forceinline__ void core_chunk(const uint8_t* st, const uint8_t* xw,
         e2m1x8_to_f16x2(lds32(tile + cl.w_off[j]), hh);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-          pa[m] = fma_f16lo(hh[0], xr[m][j][0], pa[m]);
-          pb[m] = fma_f16hi(hh[0], xr[m][j][0], pb[m]);
-          pa[m] = fma_f16lo(hh[2], xr[m][j][1], pa[m]);
-          pb[m] = fma_f16hi(hh[2], xr[m][j][1], pb[m]);
-          pc[m] = fma_f16lo(hh[1], xr[m][j][0], pc[m]);
-          pd[m] = fma_f16hi(hh[1], xr[m][j][0], pd[m]);
-          pc[m] = fma_f16lo(hh[3], xr[m][j][1], pc[m]);
-          pd[m] = fma_f16hi(hh[3], xr[m][j][1], pd[m]);
+          pa[m] = fma_f16lo(hh[0], xw[m][j][0], pa[m]);
+          pb[m] = fma_f16hi(hh[0], xw[m][j][0], pb[m]);
+          pa[m] = fma_f16lo(hh[2], xw[m][j][1], pa[m]);
+          pb[m] = fma_f16hi(hh[2], xw[m][j][1], pb[m]);
+          pc[m] = fma_f16lo(hh[1], xw[m][j][0], pc[m]);
+          pd[m] = fma_f16hi(hh[1], xw[m][j][0], pd[m]);
+          pc[m] = fma_f16lo(hh[3], xw[m][j][1], pc[m]);
+          pd[m] = fma_f16hi(hh[3], xw[m][j][1], pd[m]);
         }
       }
       const float sg = f16lo_to_f32(sp), sg8 = f16hi_to_f32(sp);  // scale * 2^-8
@@ -158,27 +156,24 @@ __device__ __forceinline__ void core_chunk(const uint8_t* st, const uint8_t* xw,
       }
     }
   } else {
-    uint32_t sgd[4], sg8d[4];  // (scale, scale) * 2^-8 per tile for rows g and g+8
+    uint32_t sgd[TN];  // (scale row g, scale row g+8) * 2^-8 per tile
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const uint32_t sw = lds_u16(st + r * kTileBytes + cl.s_off);
-      sgd[r] = scale_pair_x2<0>(sw);
-      sg8d[r] = scale_pair_x2<1>(sw);
-    }
+    for (int r = 0; r < TN; ++r) sgd[r] = scale_pair_lohi<0, 1>(lds16(st + r * kTileBytes + cl.s_off));
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint32_t x0[MT], x1[MT];
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
-        x0[m] = lds32(xw + m * kXCoreChunkBytes + cl.x_off[j]);
-        x1[m] = lds32(xw + m * kXCoreChunkBytes + cl.x_off[j] + 16);
+        x0[m] = lds32(xr[m] + cl.x_off[j]);
+        x1[m] = lds32(xr[m] + cl.x_off[j] + 16);
       }
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < TN; ++r) {
         uint32_t hh[4];
         e2m1x8_to_f16x2(lds32(st + r * kTileBytes + cl.w_off[j]), hh);
-        const uint32_t h0 = hmul2(hh[0], sgd[r]), h2 = hmul2(hh[2], sgd[r]);
-        const uint32_t h1 = hmul2(hh[1], sg8d[r]), h3 = hmul2(hh[3], sg8d[r]);
+        uint32_t h0, h1, h2, h3;
+        hmul2_bcast(hh[0], hh[1], sgd[r], h0, h1);
+        hmul2_bcast(hh[2], hh[3], sgd[r], h2, h3);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
           float a0 = acc[r][m][0], a1 = acc[r][m][1];
@@ -197,120 +192,108 @@ __device__ __forceinline__ void core_chunk(const uint8_t* st, const uint8_t* xw,
   }
 }
 
-// Shared-memory ring of one warp.
-struct Ring {
-  uint8_t* buf;    // ns * kStageBytes
-  uint64_t* bar;   // ns mbarriers
-  int ns;
+// Chunks per copy for a piece of tn tiles: a copy (one TMA box) carries tn tiles
+// of copy_chunks(tn) consecutive chunks, at most kStageBytes.
+__host__ __device__ constexpr int copy_chunks(int tn) { return tn == 1 ? 4 : (tn == 2 ? 2 : 1); }
+
+// The TMA view of a repacked weight (stack): a 4-D tensor of 8-byte elements,
+// dims (72 = one tile's 576 bytes, 4 tiles of a chunk, kc chunks, groups of
+// all matrices), so the box (72, tn, copy_chunks(tn), 1) at (0, t0, c, group)
+// is tiles t0..t0+tn-1 of chunks c, c+1, ... of one group, stored in shared
+// memory chunk-major: [chunk][tile][576 bytes].
+struct WeightMaps {
+  CUtensorMap w[4];   // the (stacked) weight; w[tn - 1] has the box of tn tiles
+  CUtensorMap sh[4];  // the shared expert of a MoE layer (unused otherwise)
 };
 
-__device__ __forceinline__ void ring_init(const Ring& r, int lane) {
-  if (lane == 0) {
-    for (int s = 0; s < r.ns; ++s) mbar_init(&r.bar[s], 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-}
+// Stage `nrows` bf16 rows of x (row_src[j] = source row, row length k) over
+// columns [col0, col0 + 64*nchunks) into shared memory as f16, row j rescaled by
+// 2^sigma[j] (sigma from the row's amax over the same columns, see
+// pow2_rescale_exponent), followed by one all-zero row (index nrows) that empty
+// token slots point at.  Row j starts at xs + j*stride.  One warp per row: the
+// lanes load the row's 16-byte groups (8 columns each), take the amax with warp
+// shuffles, then convert and store in the MMA fragment order or the CUDA-core
+// pair order.  Rows of up to 32*kStageRegs groups are read once and held in
+// registers; longer rows are read twice.  Columns at or past k are stored as
+// zeros.  All threads of the CTA call it; it ends with a __syncthreads.
+constexpr int kStageRegs = 12;
 
-// Lane 0 only: copy the chunk at `src` (kStageBytes) into stage s.
-__device__ __forceinline__ void ring_issue(const Ring& r, int s, const uint8_t* src, uint64_t policy) {
-  mbar_arrive_expect_tx(&r.bar[s], kStageBytes);
-  bulk_g2s(r.buf + s * kStageBytes, src, kStageBytes, &r.bar[s], policy);
-}
-
-// Stage the bf16 activations of SLOTS token slots over columns [col0, col0 +
-// 64*nchunks) into shared memory as f16, each slot rescaled by 2^sigma[slot]
-// (sigma from the slot's amax over the same columns, see pow2_rescale_exponent).
-// tok_row(slot) gives the source row of x (or -1 for an empty slot); k = row length.
-// Work items are (slot, 8-column group): one 16-byte load each, kStageBatch loads
-// in flight per thread.  Pass 1 takes the per-slot amax (shared-memory atomicMax
-// on the float bits, exact), pass 2 reloads (L1/L2 hits), converts and stores in
-// the MMA fragment layout or the CUDA-core pair layout (see the constants above).
-// All threads of the CTA call it; it ends with a __syncthreads.
-constexpr int kStageBatch = 8;
-
-template <bool kMMA, int SLOTS, typename TokRow>
-__device__ __forceinline__ void stage_tokens(const uint16_t* __restrict__ x, int k, int col0, int nchunks,
-                                             TokRow tok_row, unsigned* s_amax, int* sigma, uint8_t* xs) {
-  const int groups = nchunks * 8;  // 8-column groups per slot
-  const int items = SLOTS * groups;
-  if (threadIdx.x < SLOTS) s_amax[threadIdx.x] = 0u;
-  __syncthreads();
-  auto src_of = [&](int it, int& slot, int& c8) -> const uint4* {
-    slot = it / groups;
-    c8 = it - slot * groups;
-    const int col = col0 + c8 * 8;
-    const int row = tok_row(slot);
-    if (row < 0 || col >= k) return nullptr;
-    return reinterpret_cast<const uint4*>(x + static_cast<size_t>(row) * k + col);
+template <bool kMMA>
+__device__ __forceinline__ void stage_rows(const uint16_t* __restrict__ x, int k, int col0, int nchunks, int nrows,
+                                           const int* row_src, int* sigma, uint8_t* xs, int stride) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  const int groups = nchunks * 8;  // 8-column groups per row
+  const bool one_pass = groups <= 32 * kStageRegs;
+  auto amax8 = [](const uint4& v) {
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    float am = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      am = fmaxf(am, fmaxf(fabsf(__uint_as_float(w4[e] << 16)), fabsf(__uint_as_float(w4[e] & 0xFFFF0000u))));
+    return am;
   };
-  // ---- pass 1: amax per slot
-  for (int base = threadIdx.x; base < items; base += blockDim.x * kStageBatch) {
-    uint4 v[kStageBatch];
-    int sl[kStageBatch];
+  auto store8 = [&](uint8_t* rowp, int c8, const uint4& v, float sc) {
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[4];
 #pragma unroll
-    for (int j = 0; j < kStageBatch; ++j) {
-      const int it = base + j * blockDim.x;
-      int c8;
-      const uint4* src = it < items ? src_of(it, sl[j], c8) : nullptr;
-      v[j] = src ? __ldg(src) : make_uint4(0, 0, 0, 0);
-      if (!src) sl[j] = -1;
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __uint_as_float(w4[e] << 16) * sc, hi = __uint_as_float(w4[e] & 0xFFFF0000u) * sc;
+      h[e] = static_cast<uint32_t>(f32_to_f16_bits(lo)) | (static_cast<uint32_t>(f32_to_f16_bits(hi)) << 16);
     }
+    const int kcl = c8 >> 3, c64 = (c8 & 7) * 8;  // chunk, first column within the chunk
+    uint8_t* cp = rowp + kcl * kXChunkBytes;
+    if constexpr (kMMA) {
+      // columns c64..c64+7 = k-step kt, half hf, pairs t = 0..3 -> word 8t + 2kt + hf
+      uint32_t* dst = reinterpret_cast<uint32_t*>(cp) + (c64 >> 4) * 2 + ((c64 >> 3) & 1);
 #pragma unroll
-    for (int j = 0; j < kStageBatch; ++j) {
-      if (sl[j] < 0) continue;
-      const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-      float am = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        am = fmaxf(am, fmaxf(fabsf(__uint_as_float(w4[e] << 16)), fabsf(__uint_as_float(w4[e] & 0xFFFF0000u))));
-      if (am > 0.f) atomicMax(&s_amax[sl[j]], __float_as_uint(am));
+      for (int t = 0; t < 4; ++t) dst[t * 8] = h[t];
+    } else {
+      *reinterpret_cast<uint4*>(cp + c64 * 2) = make_uint4(h[0], h[1], h[2], h[3]);
     }
-  }
-  __syncthreads();
-  if (threadIdx.x < SLOTS) sigma[threadIdx.x] = pow2_rescale_exponent(__uint_as_float(s_amax[threadIdx.x]));
-  __syncthreads();
-  // ---- pass 2: convert and store
-  uint32_t* xw = reinterpret_cast<uint32_t*>(xs);
-  for (int base = threadIdx.x; base < items; base += blockDim.x * kStageBatch) {
-    uint4 v[kStageBatch];
-    int sl[kStageBatch], cg[kStageBatch];
+  };
+  for (int row = warp; row <= nrows; row += nwarps) {
+    uint8_t* rowp = xs + static_cast<size_t>(row) * stride;
+    if (row == nrows) {  // the zero row
+      for (int b = lane * 16; b < nchunks * kXChunkBytes; b += 32 * 16) *reinterpret_cast<uint4*>(rowp + b) = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint16_t* src = x + static_cast<size_t>(row_src[row]) * k + col0;
+    const int lim = k - col0;  // columns of this row that exist
+    auto load8 = [&](int c8) -> uint4 {
+      return (c8 < groups && c8 * 8 < lim) ? __ldg(reinterpret_cast<const uint4*>(src + c8 * 8)) : make_uint4(0, 0, 0, 0);
+    };
+    uint4 v[kStageRegs];
+    float am = 0.f;
+    if (one_pass) {
 #pragma unroll
-    for (int j = 0; j < kStageBatch; ++j) {
-      const int it = base + j * blockDim.x;
-      sl[j] = -1;
-      cg[j] = 0;
-      v[j] = make_uint4(0, 0, 0, 0);
-      if (it < items) {
-        // empty slots and columns past k are stored as zeros (the tile padding
-        // is zero too, but stale shared memory could hold non-finite values)
-        const uint4* src = src_of(it, sl[j], cg[j]);
-        if (src) v[j] = __ldg(src);
+      for (int j = 0; j < kStageRegs; ++j) v[j] = load8(lane + 32 * j);
+#pragma unroll
+      for (int j = 0; j < kStageRegs; ++j) am = fmaxf(am, amax8(v[j]));
+    } else {
+      for (int b = 0; b < groups; b += 32 * kStageRegs) {
+#pragma unroll
+        for (int j = 0; j < kStageRegs; ++j) v[j] = load8(b + lane + 32 * j);
+#pragma unroll
+        for (int j = 0; j < kStageRegs; ++j) am = fmaxf(am, amax8(v[j]));
       }
     }
 #pragma unroll
-    for (int j = 0; j < kStageBatch; ++j) {
-      if (sl[j] < 0) continue;  // past the last item
-      const float sc = exp2i(sigma[sl[j]]);
-      const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-      uint32_t h[4];
+    for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
+    const int sg = pow2_rescale_exponent(am);
+    if (lane == 0) sigma[row] = sg;
+    const float sc = exp2i(sg);
+    if (one_pass) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float lo = __uint_as_float(w4[e] << 16) * sc, hi = __uint_as_float(w4[e] & 0xFFFF0000u) * sc;
-        h[e] = static_cast<uint32_t>(f32_to_f16_bits(lo)) | (static_cast<uint32_t>(f32_to_f16_bits(hi)) << 16);
-      }
-      const int kcl = cg[j] >> 3, c64 = (cg[j] & 7) * 8;  // chunk, first column within the chunk
-      if constexpr (kMMA) {
-        constexpr int NT = (SLOTS + 7) / 8;
-        // columns c64..c64+7 = k-tile kt, half hf, pairs t = 0..3 -> lanes (g, t), word 2*kt + hf
-        const int kt = c64 >> 4, hf = (c64 >> 3) & 1;
-        const int nt = sl[j] >> 3, g = sl[j] & 7;
-        uint32_t* dst = xw + (static_cast<size_t>(kcl) * NT + nt) * 256 + (g * 4) * 8 + kt * 2 + hf;
+      for (int j = 0; j < kStageRegs; ++j)
+        if (lane + 32 * j < groups) store8(rowp, lane + 32 * j, v[j], sc);
+    } else {
+      for (int b = 0; b < groups; b += 32 * kStageRegs) {
 #pragma unroll
-        for (int t = 0; t < 4; ++t) dst[t * 8] = h[t];
-      } else {
-        uint4* dst = reinterpret_cast<uint4*>(xw + (static_cast<size_t>(kcl) * SLOTS + sl[j]) * 32 + c64 / 2);
-        *dst = make_uint4(h[0], h[1], h[2], h[3]);
+        for (int j = 0; j < kStageRegs; ++j) v[j] = load8(b + lane + 32 * j);
+#pragma unroll
+        for (int j = 0; j < kStageRegs; ++j)
+          if (b + lane + 32 * j < groups) store8(rowp, b + lane + 32 * j, v[j], sc);
       }
     }
   }
