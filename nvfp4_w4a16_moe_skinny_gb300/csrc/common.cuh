@@ -96,9 +96,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // given parity to complete.  Every lane observes the completion itself (so the
 // bulk-copied bytes are visible to it) and all lanes return the same answer:
 // false, with kErrWaitTimeout recorded, if the phase did not complete within
-// kWaitCycles.
+// kWaitCycles.  The first probe does not suspend: a stage is usually full
+// already.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
-  if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, 1u << 20))) return true;
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   const long long t0 = clock64();
   while (true) {
     if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, 1u << 20))) return true;
@@ -113,6 +114,27 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// The same three operations on shared-space addresses (no address conversion).
+__device__ __forceinline__ void mbar_arrive_expect_tx_s(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                           uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_s(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                              uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(policy)
+      : "memory");
 }
 
 // 1-D bulk copy global -> shared (TMA engine); completion is counted on `bar`.

@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* mul = reinterpret_cast<float*>(slot_out + kMaxCtaSegs * 16);
   float* red_v = mul + kMaxCtaSegs * 16;                                     // [kWarps * 16]
   int* red_i = reinterpret_cast<int*>(red_v + kWarps * 16);
-  int* cur = red_i + kWarps * 16 + warp * 8;                                 // [kWarps * 8] copy cursors
+  int* cur = red_i + kWarps * 16 + warp * 8;                                 // [kWarps * 8] box cursors
   int* seg_list = red_i + kWarps * 16 + kWarps * 8;                          // [n_experts + 2]
   int* misc = seg_list + p.n_experts + 2;  // [0] segments, [1] last-arrival flag, [2] staged rows
 
@@ -217,42 +217,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto slice_len = [&](int s) { return min(p.kc, (s + 1) * p.L) - s * p.L; };
 
-  // ---- producer (lane 0): cursor over this warp's pieces.  A piece of tn tiles
-  // is ceil(chunks / copy_chunks(tn)) copies; the last may run past the slice
-  // (those chunks are loaded, or zero-filled past K, and not used).  The cursor
-  // lives in shared memory (lane 0's only), not in registers: [0] next piece,
-  // [1] copies left, [2] map index (tn-1, +4 for the shared expert), [3] t0,
-  // [4] next chunk, [5] group, [6] chunks per copy.
-  if (lane == 0) cur[0] = 0, cur[1] = 0;
+  // ---- producer (lane 0): cursor over this warp's pieces.  A whole unit (four
+  // tiles) is one bulk copy of 2,304 contiguous bytes per chunk, from a source
+  // pointer held in registers; a piece of 1-3 tiles is ceil(chunks /
+  // copy_chunks(tn)) TMA boxes, whose cursor lives in shared memory (lane 0's
+  // only: [0] map index, tn-1 or +4 for the shared expert, [1] t0, [2] next
+  // chunk, [3] group, [4] chunks per copy).  The last box may run past the slice
+  // (those chunks are loaded, or zero-filled past K, and not used).
+  int pk = 0;                      // next piece to open
+  int prem = 0;                    // copies left in the open piece
+  const uint8_t* psrc = nullptr;   // next bulk-copy source; nullptr: the piece uses TMA boxes
   const uint64_t policy = l2_evict_first_policy();
   uint8_t* ring = smem + static_cast<size_t>(warp) * ns * kStageBytes;
+  const uint32_t ring_s = smem_addr(ring), bar_s = smem_addr(bar);
   auto issue_next = [&](int stage) {
-    if (cur[1] == 0) {
-      if (cur[0] >= n_pieces) return;
-      const Piece pc = piece_at(cur[0]++);
+    if (prem == 0) {
+      if (pk >= n_pieces) return;
+      const Piece pc = piece_at(pk++);
       const int e = seg_list[pc.seg];
-      const int step = copy_chunks(pc.tn);
-      cur[1] = (slice_len(pc.s) + step - 1) / step;
-      cur[2] = (pc.tn - 1) + (e == kSharedSeg ? 4 : 0);
-      cur[3] = pc.t0;
-      cur[4] = pc.s * p.L;
-      cur[5] = (e >= 0 ? e * p.ng : 0) + pc.grp;
-      cur[6] = step;
+      const int group = (e >= 0 ? e * p.ng : 0) + pc.grp;  // within the stack
+      if (pc.tn == kChunkTiles) {
+        prem = slice_len(pc.s);
+        psrc = (e == kSharedSeg ? p.w_sh : p.w) + (static_cast<size_t>(group) * p.kc + pc.s * p.L) * kStageBytes;
+      } else {
+        const int step = copy_chunks(pc.tn);
+        prem = (slice_len(pc.s) + step - 1) / step;
+        psrc = nullptr;
+        cur[0] = (pc.tn - 1) + (e == kSharedSeg ? 4 : 0);
+        cur[1] = pc.t0;
+        cur[2] = pc.s * p.L;
+        cur[3] = group;
+        cur[4] = step;
+      }
     }
-    const int mi = cur[2];
-    const uint32_t bytes = static_cast<uint32_t>(((mi & 3) + 1) * cur[6]) * kTileBytes;
-    mbar_arrive_expect_tx(&bar[stage], bytes);
-    if ((mi & 3) == 3) {
-      // four tiles of one chunk are 2,304 contiguous bytes: a plain bulk copy
-      const uint8_t* base = mi < 4 ? p.w : p.w_sh;
-      bulk_g2s(ring + stage * kStageBytes,
-               base + (static_cast<size_t>(cur[5]) * p.kc + cur[4]) * kStageBytes, kStageBytes, &bar[stage], policy);
+    const uint32_t b = bar_s + stage * 8, d = ring_s + stage * kStageBytes;
+    if (psrc) {
+      mbar_arrive_expect_tx_s(b, kStageBytes);
+      bulk_g2s_s(d, psrc, kStageBytes, b, policy);
+      psrc += kStageBytes;
     } else {
-      const CUtensorMap* map = mi < 4 ? &maps.w[mi] : &maps.sh[mi - 4];
-      tma_load_4d(ring + stage * kStageBytes, map, 0, cur[3], cur[4], cur[5], &bar[stage], policy);
+      const int mi = cur[0];
+      mbar_arrive_expect_tx_s(b, static_cast<uint32_t>(((mi & 3) + 1) * cur[4]) * kTileBytes);
+      tma_load_4d_s(d, mi < 4 ? &maps.w[mi] : &maps.sh[mi - 4], 0, cur[1], cur[2], cur[3], b, policy);
+      cur[2] += cur[4];
     }
-    cur[4] += cur[6];
-    --cur[1];
+    --prem;
   };
   if (lane == 0)
     for (int st = 0; st < ns; ++st) issue_next(st);
@@ -383,39 +392,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < NA; ++c)
 #pragma unroll
           for (int i = 0; i < NI; ++i) acc[a][c][i] = 0.f;
-      const int step = copy_chunks(pc.tn);
-      for (int ch = 0; ch < nch; ch += step) {
-        if (!mbar_wait_warp(&bar[st], ph)) {
-          failed = true;
-          break;
-        }
-        const uint32_t stage = ring_addr + st * kStageBytes;
-        const int cnt = min(step, nch - ch);  // chunks of this copy inside the slice
-        // the copy's chunks, each TN tiles at stage + cc*TN*576
-        auto consume = [&](auto tn_c) {
-          constexpr int TN = decltype(tn_c)::value;
-          for (int cc = 0; cc < cnt; ++cc) {
-            const uint32_t sub = stage + cc * TN * kTileBytes;
+      // the piece's copies; copy j holds chunks j*step .. of the slice, each TN tiles
+      // at stage + c*TN*576 (one loop per TN, chosen once per piece)
+      auto stream_piece = [&](auto tn_c) {
+        constexpr int TN = decltype(tn_c)::value;
+        constexpr int kStep = copy_chunks(TN);
+        for (int ch = 0; ch < nch; ch += kStep) {
+          if (!mbar_wait_warp(&bar[st], ph)) {
+            failed = true;
+            return;
+          }
+          const uint32_t stage = ring_addr + st * kStageBytes;
+          if constexpr (kStep == 1) {
             if constexpr (kMMA)
-              mma_chunk<NT, TN>(sub, xr, lane, acc);
+              mma_chunk<NT, TN>(stage, xr, lane, acc);
             else
-              core_chunk<MT, TN>(sub, xr, cl, acc);
+              core_chunk<MT, TN>(stage, xr, cl, acc);
 #pragma unroll
             for (int c = 0; c < NA; ++c) xr[c] += kXChunkBytes;
+          } else {
+            const int cnt = min(kStep, nch - ch);  // chunks of this copy inside the slice
+            for (int cc = 0; cc < cnt; ++cc) {
+              if constexpr (kMMA)
+                mma_chunk<NT, TN>(stage + cc * TN * kTileBytes, xr, lane, acc);
+              else
+                core_chunk<MT, TN>(stage + cc * TN * kTileBytes, xr, cl, acc);
+#pragma unroll
+              for (int c = 0; c < NA; ++c) xr[c] += kXChunkBytes;
+            }
           }
-        };
-        switch (pc.tn) {
-          case 4: consume(std::integral_constant<int, 4>{}); break;
-          case 3: consume(std::integral_constant<int, 3>{}); break;
-          case 2: consume(std::integral_constant<int, 2>{}); break;
-          default: consume(std::integral_constant<int, 1>{}); break;
+          __syncwarp();
+          if (lane == 0) {
+            fence_proxy_async_smem();  // this warp's reads of the stage before the next copy into it
+            issue_next(st);
+          }
+          if (++st == ns) st = 0, ph ^= 1u;
         }
-        __syncwarp();
-        if (lane == 0) {
-          fence_proxy_async_smem();  // this warp's reads of the stage before the next copy into it
-          issue_next(st);
-        }
-        if (++st == ns) st = 0, ph ^= 1u;
+      };
+      switch (pc.tn) {
+        case 4: stream_piece(std::integral_constant<int, 4>{}); break;
+        case 3: stream_piece(std::integral_constant<int, 3>{}); break;
+        case 2: stream_piece(std::integral_constant<int, 2>{}); break;
+        default: stream_piece(std::integral_constant<int, 1>{}); break;
       }
       if (failed) break;
       // ---- to output units (CUDA cores: first the sum over the 4 lanes of a row pair)

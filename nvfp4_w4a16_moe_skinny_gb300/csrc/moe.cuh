@@ -21,66 +21,63 @@ namespace nvfp4 {
 
 // One CTA.  Phase 1: one warp per token selects the top_k largest logits
 // (descending, ties -> lower expert id) by repeated warp arg-max and takes a
-// softmax over them.  Phase 2: a stable counting sort of the (token, slot)
-// pairs by expert with warp ballots: counts, an exclusive scan, then ranked
-// writes in ascending pair order.  No atomics.
+// softmax over them; lane r keeps the r-th choice.  Phase 2: a stable counting
+// sort of the (token, slot) pairs by expert with warp ballots: counts, a
+// block-wide exclusive scan, then ranked writes in ascending pair order.  No
+// atomics.  NPER: logits per lane (n_experts <= 32 * NPER).
 constexpr int kRouteThreads = 1024;
 
+template <int NPER>
 __global__ void __launch_bounds__(kRouteThreads, 1)
     moe_route_kernel(const float* __restrict__ logits, int m, int n_experts, int top_k, int* __restrict__ ids,
                      float* __restrict__ probs, int* __restrict__ offsets, int* __restrict__ sorted_pairs) {
   extern __shared__ int route_smem[];
-  int* s_ids = route_smem;                 // [m * top_k]
-  int* s_cnt = s_ids + m * top_k;          // [n_experts + 1]
+  const int pairs = m * top_k;
+  int* s_ids = route_smem;                 // [pairs]
+  int* s_cnt = s_ids + pairs;              // [n_experts + 1]
+  int* s_wsum = s_cnt + n_experts + 1;     // [32] per-warp totals of the scan
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
-  const int pairs = m * top_k;
   pdl_wait();  // the logits may come from the previous grid
   pdl_launch_dependents();
   for (int t = warp; t < m; t += nwarps) {
     const float* row = logits + static_cast<size_t>(t) * n_experts;
-    // the lane's logits (experts lane + 32*i), read once
-    float lv[32];
+    float lv[NPER];  // experts lane + 32*i, read once
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < NPER; ++i) {
       const int e = lane + 32 * i;
       lv[i] = e < n_experts ? __ldg(row + e) : -INFINITY;
     }
-    uint32_t taken = 0;  // bit i: expert lane + 32*i already chosen (n_experts <= 1024)
-    float chosen_v[32];
-    int chosen_e[32];
+    uint32_t taken = 0;  // bit i: expert lane + 32*i already chosen
+    float myv = -INFINITY;
+    int mye = 0;
     for (int r = 0; r < top_k; ++r) {
       float bv = -INFINITY;
       int be = 0x7FFFFFFF;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < NPER; ++i) {
         const int e = lane + 32 * i;
-        if (e < n_experts && !((taken >> i) & 1u)) {
-          const float v = lv[i];
-          if (v > bv || (v == bv && e < be)) bv = v, be = e;
-        }
+        if (e < n_experts && !((taken >> i) & 1u) && (lv[i] > bv || (lv[i] == bv && e < be))) bv = lv[i], be = e;
       }
+#pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
         const int oe = __shfl_xor_sync(0xffffffffu, be, off);
         if (ov > bv || (ov == bv && oe < be)) bv = ov, be = oe;
       }
       if (lane == (be & 31)) taken |= 1u << (be >> 5);
-      chosen_v[r] = bv;
-      chosen_e[r] = be;
+      if (lane == r) myv = bv, mye = be;
     }
-    // softmax over the chosen logits (chosen_v[0] is the maximum)
+    // softmax over the chosen logits (round 0 holds the maximum)
+    const float vmax = __shfl_sync(0xffffffffu, myv, 0);
+    const float ez = lane < top_k ? expf(myv - vmax) : 0.f;
+    float z = ez;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
     if (lane < top_k) {
-      float z = 0.f;
-      float mine = 0.f;
-      for (int r = 0; r < top_k; ++r) {
-        const float ez = expf(chosen_v[r] - chosen_v[0]);
-        z += ez;
-        if (r == lane) mine = ez;
-      }
-      ids[t * top_k + lane] = chosen_e[lane];
-      probs[t * top_k + lane] = mine / z;
-      s_ids[t * top_k + lane] = chosen_e[lane];
+      ids[t * top_k + lane] = mye;
+      probs[t * top_k + lane] = ez / z;
+      s_ids[t * top_k + lane] = mye;
     }
   }
   __syncthreads();
@@ -95,17 +92,32 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     if (lane == 0) s_cnt[e] = cnt;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int e = 0; e < n_experts; ++e) {
-      const int c = s_cnt[e];
-      s_cnt[e] = run;
-      offsets[e] = run;
-      run += c;
-    }
-    s_cnt[n_experts] = run;
-    offsets[n_experts] = run;
+  // exclusive scan of the counts: one thread per expert (n_experts <= 1024)
+  const int c = threadIdx.x < n_experts ? s_cnt[threadIdx.x] : 0;
+  int incl = c;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
   }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nwarps ? s_wsum[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += o;
+    }
+    s_wsum[lane] = w;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int excl = incl - c + (warp > 0 ? s_wsum[warp - 1] : 0);
+  if (threadIdx.x < n_experts) {
+    s_cnt[threadIdx.x] = excl;
+    offsets[threadIdx.x] = excl;
+  }
+  if (threadIdx.x == 0) offsets[n_experts] = pairs;
   __syncthreads();
   // ranked writes in ascending pair order
   for (int e = warp; e < n_experts; e += nwarps) {
