@@ -280,6 +280,26 @@ def run_ours(args, rank, world, dist):
     total_ms = t0.elapsed_time(t1)
     lm_us = 1e3 * statistics.mean(a.elapsed_time(b) for a, b in ev_lm)
 
+    # ---- the same steps replayed from a CUDA graph (one step captured; launch costs off the host)
+    graph_ms = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        for _ in range(2):
+            graph.replay()
+        stream.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            g1.record(stream)
+        stream.synchronize()
+        graph_ms = g0.elapsed_time(g1) / args.steps
+    except Exception as exc:  # capture can be unavailable; the eager number stands
+        print(f"graph replay skipped: {exc}", file=sys.stderr)
+
     # ---- per-call attribution: events around every call (no overlap across calls)
     ev = {name: timed_events() for name, _ in calls}
     with torch.cuda.stream(stream):
@@ -359,6 +379,7 @@ def run_ours(args, rank, world, dist):
                      "peak": peak, "peak_kind": f"{peak_kind} (copy)", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "graph_ms_per_step": round(graph_ms, 4) if graph_ms else None,
         "gpu_launches": launches_per_step * args.steps,
         "timing": "value: steps back to back, events around the region; kernels_us: a second pass with events "
                   "around every call",

@@ -4,10 +4,13 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <array>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "nvfp4_skinny.h"
 #include "common.cuh"
@@ -48,9 +51,19 @@ nvfp4_status check_weight(const nvfp4_weight* w, int num_matrices, uint32_t flag
   return NVFP4_OK;
 }
 
+// Allow the kernel the full opt-in shared memory, once per (kernel, device).
 template <typename K>
 cudaError_t set_smem(K kernel, size_t bytes) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, bool> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count(key)) return bytes <= kMaxSmem ? cudaSuccess : cudaErrorInvalidValue;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMaxSmem));
+  if (e == cudaSuccess) done[key] = true;
+  return e;
 }
 
 // ------------------------------------------------------------------ streaming-kernel plans
@@ -110,41 +123,45 @@ bool make_plan(int m, int S, int ng, int kc, int n_seg_max, int n_experts, bool 
 }
 
 // Predicted time (us) of one launch of `plan` over n_seg segments of ng groups,
-// on the reference grid: staging the activations, then the slowest of the
-// busiest SM's share of HBM, its dequantisation throughput and its busiest
-// warp's chain of copies (at most ns in flight), plus the fixup when K is
-// split.  Only used to rank the splits.
+// on the reference grid, for ranking the splits: a fixed launch cost, staging
+// the activations over the columns a CTA touches, the busiest warp's
+// tile-chunks (whole units amortise the x loads over four tiles and run
+// faster per tile than split tiles) or the SM's share of HBM, whichever is
+// slower, and, when K is split, a fence + ticket per piece and the last
+// slice's reads of the S partials a few at a time.  The constants are fitted to
+// measured launches of the dense and MoE products on GB300.
 double plan_cost(int m, int ng, int n_seg, bool x_by_pair, const Plan& plan) {
   const int S = plan.S, L = plan.L;
   const long long units = static_cast<long long>(n_seg) * S * ng;
   const long long nu = (units + kPlanSMs - 1) / kPlanSMs;  // units of the busiest CTA
-  // copies in the busiest warp's chain: whole units round-robin, or (fewer than
-  // 16 units) at most two pieces of its tile range, 1, 2 or 4 chunks per copy
-  long long chain;
-  if (nu >= kWarps) {
-    chain = (nu + kWarps - 1) / kWarps * L;
-  } else {
-    const int tiles = static_cast<int>(std::max<long long>(1, (4 * nu + kWarps - 1) / kWarps));
-    chain = tiles >= 3 ? 2 * L : (L + copy_chunks(tiles) - 1) / copy_chunks(tiles);
+  const bool mma = use_mma(m);
+  long long pieces, tile_chunks;
+  double per_tc;
+  if (nu >= kWarps) {  // whole units round-robin
+    pieces = (nu + kWarps - 1) / kWarps;
+    tile_chunks = pieces * kChunkTiles * L;
+    per_tc = mma ? 0.26 : 0.22;
+  } else {  // the units' tiles spread over the warps
+    const long long tiles = (kChunkTiles * nu + kWarps - 1) / kWarps;
+    pieces = std::min<long long>(2, tiles);
+    tile_chunks = tiles * L;
+    per_tc = mma ? 0.30 : 0.25;
   }
   const int rows = x_by_pair ? m * std::min(plan.max_cta_segs, 2) : m;
-  const double t_stage = 1.0 + static_cast<double>(rows) * plan.xs_chunks * kXChunkBytes / 20000.0;
-  const double tiles_per_us = use_mma(m) ? 65.0 : (m <= 2 ? 90.0 : 220.0 / (m + 1));
-  const double copy_us = std::max(0.22, 1.3 / plan.ns);  // one warp's copies, ns in flight
+  const double span = std::min<double>(plan.xs_chunks, L * (1.0 + static_cast<double>(nu - 1) / ng));
+  const double t_stage = 1.0 + rows * span * kXChunkBytes / 30000.0;
+  const double t_warp = tile_chunks * per_tc;
   const double t_mem = static_cast<double>(nu) * L * kStageBytes / 40000.0;  // 40 GB/s per SM
-  const double t_alu = static_cast<double>(nu) * 4 * L / tiles_per_us;
-  const double t_lat = static_cast<double>(chain) * copy_us;
-  // fixup: a fence and a ticket, then the last slice reads the S partials a few at a time
   const int v = acc_per_tile(m), batch = v >= 12 ? 1 : (v >= 8 ? 2 : 4);
-  const double t_fix = S > 1 ? 1.2 + 0.35 * ((S + batch - 1) / batch) : 0.0;
-  return t_stage + std::max(t_mem, std::max(t_alu, t_lat)) + t_fix;
+  const double t_fix = S > 1 ? 1.5 * pieces + 1.5 * ((S + batch - 1) / batch) : 0.0;
+  return 3.0 + t_stage + std::max(t_warp, t_mem) + t_fix;
 }
 
 // S for a job: the cheapest by plan_cost (ties to the smaller S), planned on the
 // reference grid so that it depends on the shapes only.  n_seg_est is the
 // expected number of segments, n_seg_max the most there can be.
-int choose_split(int m, int ng, int kc, int n_seg_est, int n_seg_max, int n_experts, bool x_by_pair,
-                 bool allow_split) {
+int choose_split_uncached(int m, int ng, int kc, int n_seg_est, int n_seg_max, int n_experts, bool x_by_pair,
+                          bool allow_split) {
   int best = 1;
   double best_cost = 1e30;
   Plan pl;
@@ -157,9 +174,26 @@ int choose_split(int m, int ng, int kc, int n_seg_est, int n_seg_max, int n_expe
     if (ceil_div(kc, L) != s) continue;  // the same slices as a smaller S
     if (!make_plan(m, s, ng, kc, n_seg_max, n_experts, x_by_pair, kPlanSMs, &pl)) continue;
     const double c = plan_cost(m, ng, n_seg_est, x_by_pair, pl);
-    if (c < best_cost * 0.97) best = s, best_cost = c;
+    if (c < best_cost * 0.99) best = s, best_cost = c;
   }
   return best;
+}
+
+// choose_split, remembered per argument set (it depends on the shapes only).
+int choose_split(int m, int ng, int kc, int n_seg_est, int n_seg_max, int n_experts, bool x_by_pair, bool allow_split) {
+  static std::mutex mu;
+  static std::map<std::array<int, 8>, int> memo;
+  const std::array<int, 8> key{m, ng, kc, n_seg_est, n_seg_max, n_experts, x_by_pair ? 1 : 0, allow_split ? 1 : 0};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = memo.find(key);
+    if (it != memo.end()) return it->second;
+  }
+  const int s = choose_split_uncached(m, ng, kc, n_seg_est, n_seg_max, n_experts, x_by_pair, allow_split);
+  std::lock_guard<std::mutex> lock(mu);
+  if (memo.size() > 4096) memo.clear();
+  memo[key] = s;
+  return s;
 }
 
 // ------------------------------------------------------------------ TMA tensor maps
@@ -201,10 +235,38 @@ bool encode_weight_maps(const nvfp4_weight* w, CUtensorMap (&maps)[4]) {
   return true;
 }
 
+// The maps of one weight, remembered per (device, address, shape): a weight is
+// repacked once and used for many calls.  The cache holds encodings only (no
+// device memory); at most 1024 entries, then it starts over.
+bool weight_maps_cached(const nvfp4_weight* w, CUtensorMap (&maps)[4]) {
+  struct Entry {
+    CUtensorMap m[4];
+  };
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, int, int, int>, Entry> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const auto key = std::make_tuple(dev, w->data, w->n, w->k, w->num_matrices);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) {
+      for (int i = 0; i < 4; ++i) maps[i] = it->second.m[i];
+      return true;
+    }
+  }
+  if (!encode_weight_maps(w, maps)) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() >= 1024) cache.clear();
+  Entry& e = cache[key];
+  for (int i = 0; i < 4; ++i) e.m[i] = maps[i];
+  return true;
+}
+
 // Maps of a weight and, for a MoE layer, of its shared expert.
 bool make_maps(const nvfp4_weight* w, const nvfp4_weight* shared, WeightMaps* out) {
-  if (!encode_weight_maps(w, out->w)) return false;
-  if (shared) return encode_weight_maps(shared, out->sh);
+  if (!weight_maps_cached(w, out->w)) return false;
+  if (shared) return weight_maps_cached(shared, out->sh);
   for (int i = 0; i < 4; ++i) out->sh[i] = out->w[i];
   return true;
 }
