@@ -101,6 +101,14 @@ __host__ __device__ inline size_t stream_smem_bytes(int xs_rows, int xs_chunks, 
   return ring + bars + xs + stream_table_bytes(n_experts);
 }
 
+// Whole-unit dealing for a CTA of nu units: the busiest warp then streams
+// ceil(nu/16) units of four tiles, against ceil(4nu/16) split tiles otherwise.
+__host__ __device__ inline bool deal_whole(long long nu) {
+  const long long whole = (nu + kWarps - 1) / kWarps * 4 * 100;
+  const long long split = (4 * nu + kWarps - 1) / kWarps * 115;
+  return whole <= split;
+}
+
 __device__ __forceinline__ bool better(float v, int r, float bv, int br) {
   return v > bv || (v == bv && r < br);
 }
@@ -189,9 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nsc_used = nu > 0 ? nsc : 0;
   if (nu == 0) c_lo = c_hi = 0;  // nothing to stage
 
-  // ---- warp w's pieces: with at least 16 units, whole units round-robin (warp w
-  // takes units w, w+16, ...); with fewer, the units' tiles as contiguous ranges
-  const bool whole = nu >= kWarps;
+  // ---- warp w's pieces: whole units round-robin (warp w takes units w, w+16,
+  // ...), or the units' tiles as contiguous ranges, whichever leaves the busiest
+  // warp less work (a split tile costs ~1.15x a tile of a whole unit: its x
+  // fragments and scale work are not shared by four tiles)
+  const bool whole = deal_whole(nu);
   struct Piece {
     int seg, s, grp, t0, tn;
   };

@@ -137,7 +137,7 @@ double plan_cost(int m, int ng, int n_seg, bool x_by_pair, const Plan& plan) {
   const bool mma = use_mma(m);
   long long pieces, tile_chunks;
   double per_tc;
-  if (nu >= kWarps) {  // whole units round-robin
+  if (deal_whole(nu)) {  // whole units round-robin
     pieces = (nu + kWarps - 1) / kWarps;
     tile_chunks = pieces * kChunkTiles * L;
     per_tc = mma ? 0.26 : 0.22;
