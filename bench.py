@@ -312,6 +312,8 @@ def run_ours(args, rank, world, dist):
     stream.synchronize()
     kernel_us = {name: 1e3 * statistics.mean(a.elapsed_time(b) for a, b in ev[name]) for name, _ in calls}
 
+    prefill = time_prefill(lib, wl, args, dev, stream) if args.prefill_m > 0 else None
+
     # ---- end to end through the public API with host buffers (copies inside the timed region)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
@@ -380,6 +382,7 @@ def run_ours(args, rank, world, dist):
                      "frac": round(achieved / peak, 4), "traffic": traffic},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "graph_ms_per_step": round(graph_ms, 4) if graph_ms else None,
+        "prefill": prefill,
         "gpu_launches": launches_per_step * args.steps,
         "timing": "value: steps back to back, events around the region; kernels_us: a second pass with events "
                   "around every call",
@@ -388,6 +391,51 @@ def run_ours(args, rank, world, dist):
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         result["cpu_baseline"] = cpu_baseline(m, seconds=args.cpu_seconds)
     return result
+
+
+def time_prefill(lib, wl, args, dev, stream):
+    """The MoE layer on a prefill chunk of `args.prefill_m` tokens (same weights as the
+    decode step): router + grouped gate+up + grouped down + combine, timed back to back
+    with events on the launching stream.  Weight-GB/s counts every expert the routing
+    touches once, plus the shared expert."""
+    import torch
+    from nvfp4_w4a16_moe_skinny_gb300 import workloads as W
+
+    m = args.prefill_m
+    mc = W.MoECase(m=m)
+    xb, _ = mc.x()
+    x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+    logits = torch.from_numpy(mc.logits()).to(dev)
+    route = (torch.empty((m, W.TOP_K), dtype=torch.int32, device=dev),
+             torch.empty((m, W.TOP_K), dtype=torch.float32, device=dev),
+             torch.empty((W.N_EXPERTS + 1,), dtype=torch.int32, device=dev),
+             torch.empty((m * W.TOP_K,), dtype=torch.int32, device=dev))
+    out = torch.empty((m, W.HIDDEN), dtype=torch.bfloat16, device=dev)
+    fn = lib.plan_moe(x, logits, W.TOP_K, wl["gate_up"], wl["down"], wl["sh_gate_up"], wl["sh_down"], route, out,
+                      stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            fn()
+    stream.synchronize()
+    counts = (route[2][1:] - route[2][:-1]).cpu()
+    active = int((counts > 0).sum())
+    nbytes = step_bytes(wl, active)["moe"]
+    steps = max(args.steps, 10)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+    stream.synchronize()
+    if lib.device_error() != 0:
+        raise RuntimeError("device error flag set during the prefill timing")
+    ms = e0.elapsed_time(e1) / steps
+    peak, _ = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"m": m, "ms_per_layer": round(ms, 4), "tokens_per_s": round(m / (ms * 1e-3), 1),
+            "weight_bytes": nbytes, "active_experts": active, "max_pairs_per_expert": int(counts.max()),
+            "weight_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4), "launches_per_layer": 4}
 
 
 def load_traffic(kernel, m):
@@ -497,6 +545,8 @@ def main():
     ap.add_argument("--m", type=int, default=15)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--prefill-m", type=int, default=512,
+                    help="also time the MoE layer on a prefill chunk of this many tokens (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -28,6 +28,13 @@ constexpr unsigned kErrWaitTimeout = 1u;
 // ~1 s at 2 GHz: far above any legitimate wait for a bulk copy.
 constexpr long long kWaitCycles = 2000000000ll;
 
+// Bytes of dynamic shared memory this launch was given.
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

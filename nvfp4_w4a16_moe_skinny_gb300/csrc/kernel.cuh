@@ -87,6 +87,7 @@ struct Job {
   int xs_chunks;          // staged-activation capacity: chunks per row
   int xs_rows;            // staged-activation capacity: rows (plus the zero row)
   int max_cta_segs;       // segments one CTA may touch (<= kMaxCtaSegs)
+  int max_segs;           // prefill kernel: capacity of the segment list
 };
 
 __host__ __device__ inline size_t stream_table_bytes(int n_experts) {

@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <array>
 #include <cstdint>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <map>
@@ -16,6 +17,7 @@
 #include "common.cuh"
 #include "quant.cuh"
 #include "kernel.cuh"
+#include "prefill.cuh"
 #include "moe.cuh"
 
 namespace nvfp4 {
@@ -75,7 +77,8 @@ constexpr int kPlanSMs = 152;
 constexpr int kMaxSplit = 16;
 
 struct Plan {
-  int S, L, ns, xs_chunks, xs_rows, max_cta_segs, grid;
+  int S, L, ns, xs_chunks, xs_rows, max_cta_segs, grid, max_segs;
+  bool per_run;
   size_t smem;
 };
 
@@ -91,35 +94,46 @@ constexpr size_t kFixCounterBytes = 256 * 1024;
 
 size_t fixup_bytes(int m, int S, int ng, int n_seg_max) {
   if (S <= 1) return 0;
-  return kFixCounterBytes + static_cast<size_t>(n_seg_max) * ng * 4 * S * 32 * acc_per_tile(m) * sizeof(float);
+  return kFixCounterBytes +
+         static_cast<size_t>(n_seg_max) * ng * 4 * S * 32 * acc_per_tile(std::min(m, 16)) * sizeof(float);
 }
 
 // Launch plan for split S on a grid of multiples of `sms` CTAs: one CTA per SM
-// (more, in waves, if a CTA would otherwise hold units of more than kMaxCtaSegs
-// segments -- only on devices with few SMs), staging capacities that cover the
-// busiest CTA, then the deepest ring that fits in shared memory.
-bool make_plan(int m, int S, int ng, int kc, int n_seg_max, int n_experts, bool x_by_pair, int sms, Plan* out) {
+// (more, in waves, if a CTA would otherwise stage the rows of more than
+// kMaxCtaSegs segments, or more rows than fit beside a ring -- only on devices
+// with few SMs), staging capacities that cover the busiest CTA, then the deepest
+// ring that fits in shared memory.
+// n_seg_max is the most segments the job can have (the capacity of the
+// segment list); n_experts sizes the decode kernel's expert table; per_run: the
+// prefill kernel, which stages one segment's 16 rows at a time.
+bool make_plan(int m, int S, int ng, int kc, int n_seg_max, int n_experts, bool per_run, bool x_by_pair, int sms,
+               Plan* out) {
   const int L = ceil_div(kc, S);
   const int per_seg = S * ng;
-  int grid = sms;
-  long long nu_max = 0;
-  int segs = 0;
-  for (;; grid += sms) {
-    nu_max = (static_cast<long long>(n_seg_max) * per_seg + grid - 1) / grid;
-    segs = static_cast<int>(std::min<long long>(n_seg_max, (nu_max + per_seg - 1) / per_seg + 1));
-    if (segs <= kMaxCtaSegs) break;
-  }
-  int xs_chunks = kc;
-  if (segs == 1) xs_chunks = static_cast<int>(std::min<long long>(kc, ((nu_max + ng - 1) / ng + 1) * L));
-  const int xs_rows = x_by_pair ? segs * m : m;
-  for (int ns = 8; ns >= 2; --ns) {
-    const size_t smem = stream_smem_bytes(xs_rows, xs_chunks, ns, n_experts);
-    if (smem <= kMaxSmem) {
-      *out = Plan{S, L, ns, xs_chunks, xs_rows, segs, grid, smem};
-      return true;
+  int prev_segs = -1;
+  for (int grid = sms;; grid += sms) {
+    const long long nu_max = (static_cast<long long>(n_seg_max) * per_seg + grid - 1) / grid;
+    const int segs = static_cast<int>(std::min<long long>(n_seg_max, (nu_max + per_seg - 1) / per_seg + 1));
+    if (!per_run && segs > kMaxCtaSegs) continue;
+    int xs_chunks = kc;
+    if (segs == 1 || per_run) {
+      const long long nu_seg = std::min<long long>(nu_max, per_seg);  // units of one run
+      xs_chunks = static_cast<int>(std::min<long long>(kc, ((nu_seg + ng - 1) / ng + 1) * L));
     }
+    const int xs_rows = per_run ? 16 : (x_by_pair ? segs * std::min(m, 16) : m);
+    for (int ns = 8; ns >= 2; --ns) {
+      const size_t smem = per_run ? prefill_smem_bytes(xs_chunks, ns, n_seg_max)
+                                  : stream_smem_bytes(xs_rows, xs_chunks, ns, n_experts);
+      if (smem <= kMaxSmem) {
+        *out = Plan{S, L, ns, xs_chunks, xs_rows, std::min(segs, kMaxCtaSegs), grid, n_seg_max, per_run, smem};
+        return true;
+      }
+    }
+    // staging the rows of fewer segments per CTA (a larger grid) is the only
+    // way left to fit; stop once the grid no longer lowers the count
+    if (!x_by_pair || per_run || segs == prev_segs) return false;
+    prev_segs = segs;
   }
-  return false;
 }
 
 // Predicted time (us) of one launch of `plan` over n_seg segments of ng groups,
@@ -130,7 +144,8 @@ bool make_plan(int m, int S, int ng, int kc, int n_seg_max, int n_experts, bool 
 // slower, and, when K is split, a fence + ticket per piece and the last
 // slice's reads of the S partials a few at a time.  The constants are fitted to
 // measured launches of the dense and MoE products on GB300.
-double plan_cost(int m, int ng, int n_seg, bool x_by_pair, const Plan& plan) {
+double plan_cost(int m_tokens, int ng, int n_seg, bool x_by_pair, const Plan& plan) {
+  const int m = std::min(m_tokens, 16);  // token slots of one segment
   const int S = plan.S, L = plan.L;
   const long long units = static_cast<long long>(n_seg) * S * ng;
   const long long nu = (units + kPlanSMs - 1) / kPlanSMs;  // units of the busiest CTA
@@ -147,7 +162,7 @@ double plan_cost(int m, int ng, int n_seg, bool x_by_pair, const Plan& plan) {
     tile_chunks = tiles * L;
     per_tc = mma ? 0.30 : 0.25;
   }
-  const int rows = x_by_pair ? m * std::min(plan.max_cta_segs, 2) : m;
+  const int rows = plan.per_run ? 16 : (x_by_pair ? m * std::min(plan.max_cta_segs, 2) : m);
   const double span = std::min<double>(plan.xs_chunks, L * (1.0 + static_cast<double>(nu - 1) / ng));
   const double t_stage = 1.0 + rows * span * kXChunkBytes / 30000.0;
   const double t_warp = tile_chunks * per_tc;
@@ -160,19 +175,19 @@ double plan_cost(int m, int ng, int n_seg, bool x_by_pair, const Plan& plan) {
 // S for a job: the cheapest by plan_cost (ties to the smaller S), planned on the
 // reference grid so that it depends on the shapes only.  n_seg_est is the
 // expected number of segments, n_seg_max the most there can be.
-int choose_split_uncached(int m, int ng, int kc, int n_seg_est, int n_seg_max, int n_experts, bool x_by_pair,
-                          bool allow_split) {
+int choose_split_uncached(int m, int ng, int kc, int n_seg_est, int n_seg_max, int n_experts, bool per_run,
+                          bool x_by_pair, bool allow_split) {
   int best = 1;
   double best_cost = 1e30;
   Plan pl;
-  if (make_plan(m, 1, ng, kc, n_seg_max, n_experts, x_by_pair, kPlanSMs, &pl))
+  if (make_plan(m, 1, ng, kc, n_seg_max, n_experts, per_run, x_by_pair, kPlanSMs, &pl))
     best_cost = plan_cost(m, ng, n_seg_est, x_by_pair, pl);
   if (!allow_split) return 1;
   if (static_cast<size_t>(n_seg_max) * ng * 4 > kFixCounterBytes / sizeof(unsigned)) return 1;
   for (int s = 2; s <= std::min(kMaxSplit, kc); ++s) {
     const int L = ceil_div(kc, s);
     if (ceil_div(kc, L) != s) continue;  // the same slices as a smaller S
-    if (!make_plan(m, s, ng, kc, n_seg_max, n_experts, x_by_pair, kPlanSMs, &pl)) continue;
+    if (!make_plan(m, s, ng, kc, n_seg_max, n_experts, per_run, x_by_pair, kPlanSMs, &pl)) continue;
     const double c = plan_cost(m, ng, n_seg_est, x_by_pair, pl);
     if (c < best_cost * 0.99) best = s, best_cost = c;
   }
@@ -180,16 +195,18 @@ int choose_split_uncached(int m, int ng, int kc, int n_seg_est, int n_seg_max, i
 }
 
 // choose_split, remembered per argument set (it depends on the shapes only).
-int choose_split(int m, int ng, int kc, int n_seg_est, int n_seg_max, int n_experts, bool x_by_pair, bool allow_split) {
+int choose_split(int m, int ng, int kc, int n_seg_est, int n_seg_max, int n_experts, bool per_run, bool x_by_pair,
+                 bool allow_split) {
   static std::mutex mu;
-  static std::map<std::array<int, 8>, int> memo;
-  const std::array<int, 8> key{m, ng, kc, n_seg_est, n_seg_max, n_experts, x_by_pair ? 1 : 0, allow_split ? 1 : 0};
+  static std::map<std::array<int, 9>, int> memo;
+  const std::array<int, 9> key{m,         ng, kc, n_seg_est, n_seg_max, n_experts, per_run ? 1 : 0, x_by_pair ? 1 : 0,
+                               allow_split ? 1 : 0};
   {
     std::lock_guard<std::mutex> lock(mu);
     const auto it = memo.find(key);
     if (it != memo.end()) return it->second;
   }
-  const int s = choose_split_uncached(m, ng, kc, n_seg_est, n_seg_max, n_experts, x_by_pair, allow_split);
+  const int s = choose_split_uncached(m, ng, kc, n_seg_est, n_seg_max, n_experts, per_run, x_by_pair, allow_split);
   std::lock_guard<std::mutex> lock(mu);
   if (memo.size() > 4096) memo.clear();
   memo[key] = s;
@@ -297,9 +314,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-template <int MT, bool kMMA, int kEpi>
-nvfp4_status launch_stream(Job p, const WeightMaps& maps, const Plan& plan, cudaStream_t stream) {
-  auto kernel = stream_kernel<MT, kMMA, kEpi>;
+nvfp4_status launch_planned(void (*kernel)(Job, WeightMaps), Job p, const WeightMaps& maps, const Plan& plan,
+                            cudaStream_t stream) {
   if (set_smem(kernel, plan.smem) != cudaSuccess) return NVFP4_ERR_CUDA;
   p.S = plan.S;
   p.L = plan.L;
@@ -307,13 +323,23 @@ nvfp4_status launch_stream(Job p, const WeightMaps& maps, const Plan& plan, cuda
   p.xs_chunks = plan.xs_chunks;
   p.xs_rows = plan.xs_rows;
   p.max_cta_segs = plan.max_cta_segs;
+  p.max_segs = plan.max_segs;
   if (launch_pdl(kernel, dim3(plan.grid), dim3(kThreads), plan.smem, stream, p, maps) != cudaSuccess)
     return NVFP4_ERR_CUDA;
   return launched();
 }
 
+template <int MT, bool kMMA, int kEpi>
+nvfp4_status launch_stream(const Job& p, const WeightMaps& maps, const Plan& plan, cudaStream_t stream) {
+  return launch_planned(stream_kernel<MT, kMMA, kEpi>, p, maps, plan, stream);
+}
+
+// The decode kernel for m <= 16 (specialised on m), the prefill kernel for a
+// grouped product planned with per-segment runs.
 template <int kEpi>
 nvfp4_status dispatch_stream(const Job& p, const WeightMaps& maps, const Plan& plan, cudaStream_t stream) {
+  if constexpr (kEpi == kEpiGated || kEpi == kEpiRows)
+    if (plan.per_run) return launch_planned(prefill_kernel<kEpi>, p, maps, plan, stream);
   switch (p.m) {
     case 1: return launch_stream<1, false, kEpi>(p, maps, plan, stream);
     case 2: return launch_stream<2, false, kEpi>(p, maps, plan, stream);
@@ -344,7 +370,7 @@ Job dense_job(const nvfp4_weight* w, const uint16_t* x, int m) {
 }
 
 int dense_split(int m, int n, int k) {
-  return choose_split(m, ceil_div(n, kGroupRows), ceil_div(k, kTileK), 1, 1, 0, false, true);
+  return choose_split(m, ceil_div(n, kGroupRows), ceil_div(k, kTileK), 1, 1, 0, false, false, true);
 }
 
 }  // namespace
@@ -445,7 +471,8 @@ nvfp4_status nvfp4_gemm(const nvfp4_weight* w, const uint16_t* x, int32_t m, uin
   p.y_ld = w->n;
   set_fixup(&p, ws);
   Plan plan;
-  if (!make_plan(m, dense_split(m, w->n, w->k), p.ng, p.kc, 1, 0, false, std::max(1, sm_count()), &plan)) return NVFP4_ERR_SHAPE;
+  if (!make_plan(m, dense_split(m, w->n, w->k), p.ng, p.kc, 1, 0, false, false, std::max(1, sm_count()), &plan))
+    return NVFP4_ERR_SHAPE;
   WeightMaps maps;
   if (!make_maps(w, nullptr, &maps)) return NVFP4_ERR_CUDA;
   return dispatch_stream<kEpiStore>(p, maps, plan, stream);
@@ -471,7 +498,7 @@ nvfp4_status lm_head_launch(const nvfp4_weight* w, const uint16_t* x, int32_t m,
   p.max_logit = max_logit;
   p.argmax = argmax;
   Plan plan;
-  if (!make_plan(m, 1, p.ng, p.kc, 1, 0, false, std::max(1, sm_count()), &plan)) return NVFP4_ERR_SHAPE;
+  if (!make_plan(m, 1, p.ng, p.kc, 1, 0, false, false, std::max(1, sm_count()), &plan)) return NVFP4_ERR_SHAPE;
   WeightMaps maps;
   if (!make_maps(w, nullptr, &maps)) return NVFP4_ERR_CUDA;
   return dispatch_stream<kEpiArgmax>(p, maps, plan, stream);
@@ -502,27 +529,43 @@ namespace {
 
 size_t align16(size_t b) { return (b + 15) & ~static_cast<size_t>(15); }
 
-// Expected number of experts that receive at least one of the m*top_k pairs
-// (uniform routing), plus the shared expert: the planning estimate of segments.
+// Segments of a MoE job: each expert that received pairs contributes one
+// segment per block of at most 16 of its pairs (one block when m <= 16), the
+// shared expert one per block of at most 16 tokens.  expected_segments is the
+// planning estimate under uniform routing (each expert's count binomial), and
+// max_segments the most any routing can produce.
 int expected_segments(int m, int top_k, int n_experts, bool shared) {
-  double miss = 1.0;
-  for (int t = 0; t < m; ++t) miss *= 1.0 - static_cast<double>(top_k) / n_experts;
-  const int est = static_cast<int>(n_experts * (1.0 - miss) + 0.5);
-  return std::max(1, std::min(est, n_experts)) + (shared ? 1 : 0);
+  const double q = static_cast<double>(top_k) / n_experts;
+  double blocks = 0.0, pmf = std::pow(1.0 - q, m);  // P(count = 0)
+  for (int c = 1; c <= m; ++c) {
+    pmf *= (static_cast<double>(m - c + 1) / c) * (q / (1.0 - q));
+    blocks += pmf * ((c + 15) / 16);
+    if (c > 64 && pmf < 1e-12) break;
+  }
+  const int est = static_cast<int>(n_experts * blocks + 0.5);
+  return std::max(1, est) + (shared ? (m + 15) / 16 : 0);
+}
+
+int max_segments(int m, int top_k, int n_experts, bool shared) {
+  const int pairs = m * top_k;
+  const int experts = std::min(n_experts, pairs) + (m > 16 ? (pairs + 15) / 16 : 0);
+  return experts + (shared ? (m + 15) / 16 : 0);
 }
 
 struct MoESplits {
   int s_gu, s_dn, n_seg_max;
+  bool per_run;  // both products stage each segment's rows in turn (m > 16)
 };
 
 MoESplits moe_splits(int m, int top_k, int n_experts, int d, int inter, bool shared) {
   const int n_seg_est = expected_segments(m, top_k, n_experts, shared);
   MoESplits r;
-  r.n_seg_max = std::min(n_experts, m * top_k) + (shared ? 1 : 0);
+  r.n_seg_max = max_segments(m, top_k, n_experts, shared);
+  r.per_run = m > 16;
   r.s_gu = choose_split(m, ceil_div(2 * inter, kGroupRows), ceil_div(d, kTileK), n_seg_est, r.n_seg_max, n_experts,
-                        false, true);
+                        r.per_run, false, true);
   r.s_dn = choose_split(m, ceil_div(d, kGroupRows), ceil_div(inter, kTileK), n_seg_est, r.n_seg_max, n_experts,
-                        true, true);
+                        r.per_run, true, true);
   return r;
 }
 
@@ -575,7 +618,7 @@ nvfp4_status moe_route_topk(const float* logits, int32_t m, int32_t n_experts, i
 }
 
 size_t moe_ffn_workspace_bytes(int32_t m, int32_t top_k, int32_t n_experts, int32_t d, int32_t inter) {
-  if (m < 1 || m > 16 || top_k < 1 || n_experts < top_k || d < 64 || inter < 32) return 0;
+  if (m < 1 || m > 4096 || top_k < 1 || n_experts < top_k || m * top_k > 16384 || d < 64 || inter < 32) return 0;
   return moe_workspace(m, top_k, n_experts, d, inter, true).total;
 }
 
@@ -599,7 +642,8 @@ nvfp4_status moe_ffn_grouped(const uint16_t* x, int32_t m, int32_t top_k, const 
     if (shared_gate_up->n != 2 * inter || shared_gate_up->k != d || shared_down->n != d || shared_down->k != inter)
       return NVFP4_ERR_SHAPE;
   }
-  if (m < 1 || m > 16 || top_k < 1 || top_k > n_exp || (d % 64) || (inter % 64)) return NVFP4_ERR_SHAPE;
+  if (m < 1 || m > 4096 || top_k < 1 || top_k > n_exp || m * top_k > 16384 || (d % 64) || (inter % 64))
+    return NVFP4_ERR_SHAPE;
   if (!aligned(x, 16) || !aligned(out, 4) || !aligned(probs, 4)) return NVFP4_ERR_ALIGN;
   if (!ws || ws_bytes < moe_ffn_workspace_bytes(m, top_k, n_exp, d, inter)) return NVFP4_ERR_WORKSPACE;
   if (!aligned(ws, 16)) return NVFP4_ERR_ALIGN;
@@ -624,7 +668,8 @@ nvfp4_status moe_ffn_grouped(const uint16_t* x, int32_t m, int32_t top_k, const 
   a.y = h, a.y_ld = inter;
   set_fixup(&a, base + wl.h + wl.d);
   Plan pa;
-  if (!make_plan(m, sp.s_gu, a.ng, a.kc, sp.n_seg_max, n_exp, false, std::max(1, sm_count()), &pa)) return NVFP4_ERR_SHAPE;
+  if (!make_plan(m, sp.s_gu, a.ng, a.kc, sp.n_seg_max, n_exp, sp.per_run, false, std::max(1, sm_count()), &pa))
+    return NVFP4_ERR_SHAPE;
   WeightMaps ma;
   if (!make_maps(gate_up, shared ? shared_gate_up : nullptr, &ma)) return NVFP4_ERR_CUDA;
   if (const nvfp4_status st = dispatch_stream<kEpiGated>(a, ma, pa, stream)) return st;
@@ -643,7 +688,8 @@ nvfp4_status moe_ffn_grouped(const uint16_t* x, int32_t m, int32_t top_k, const 
   b.yf = dpart, b.yf_ld = d;
   set_fixup(&b, base + wl.h + wl.d);
   Plan pb;
-  if (!make_plan(m, sp.s_dn, b.ng, b.kc, sp.n_seg_max, n_exp, true, std::max(1, sm_count()), &pb)) return NVFP4_ERR_SHAPE;
+  if (!make_plan(m, sp.s_dn, b.ng, b.kc, sp.n_seg_max, n_exp, sp.per_run, true, std::max(1, sm_count()), &pb))
+    return NVFP4_ERR_SHAPE;
   WeightMaps mb;
   if (!make_maps(down, shared ? shared_down : nullptr, &mb)) return NVFP4_ERR_CUDA;
   if (const nvfp4_status st = dispatch_stream<kEpiRows>(b, mb, pb, stream)) return st;

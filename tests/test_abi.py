@@ -60,7 +60,10 @@ def test_sizes_reject_bad_shapes(so):
     assert so.nvfp4_repacked_bytes(0, 64, 1) == 0
     assert so.nvfp4_gemm_workspace_bytes(17, 64, 64) == 0   # m > 16
     assert so.lm_head_workspace_bytes(0, 100) == 0
-    assert so.moe_ffn_workspace_bytes(17, 8, 128, 2816, 704) == 0        # m > 16
+    assert so.moe_ffn_workspace_bytes(4097, 1, 128, 2816, 704) == 0      # m > 4096
+    assert so.moe_ffn_workspace_bytes(2049, 8, 128, 2816, 704) == 0      # m * top_k > 16384
+    # a prefill chunk (m > 16) is planned like decode, one 16-token block per segment
+    assert so.moe_ffn_workspace_bytes(512, 8, 128, 2816, 704) >= (512 * 8 + 512) * (704 * 2 + 2816 * 4)
     # h (bf16) and the per-(token, slot) down outputs (fp32) are always part of it
     assert so.moe_ffn_workspace_bytes(15, 8, 128, 2816, 704) >= (15 * 8 + 15) * (704 * 2 + 2816 * 4)
 

@@ -74,7 +74,9 @@ def _experts(lib, case, shared):
     return _EXPERTS[key]
 
 
-def _moe_case(lib, m, d, inter, n_exp, top_k, shared, tag, logits=None):
+def _moe_case(lib, m, d, inter, n_exp, top_k, shared, tag, logits=None, rows=None):
+    """Run the layer on the GPU for all m tokens; the oracle computes the tokens in
+    `rows` (all by default) -- a token's output depends on its own x and logits only."""
     case = W.MoECase(m=m, d=d, inter=inter, n_experts=n_exp, top_k=top_k, tag=tag)
     gu, dn, wgu, wdn, sgu, sdn = _experts(lib, case, shared)
     xb, xf = case.x()
@@ -84,7 +86,11 @@ def _moe_case(lib, m, d, inter, n_exp, top_k, shared, tag, logits=None):
     ids, probs, offsets, pairs = lib.route_topk(upload_f32(logits), top_k)
     out = lib.moe_ffn(x, top_k, probs, offsets, pairs, wgu, wdn, sgu, sdn)
     torch.cuda.synchronize()
-    # oracle: quantize only the experts the routing uses (plus the shared one)
+    got = bf16_to_f64(out)
+    if rows is not None:
+        rows = np.asarray(rows)
+        xf, logits, got = xf[rows], logits[rows], got[rows]
+    # oracle: quantize only the experts the (sampled) routing uses, plus the shared one
     oids, _ = OM.route_topk(logits, top_k)
     used = sorted(set(oids.reshape(-1).tolist()))
     gq = [None] * n_exp
@@ -101,12 +107,14 @@ def _moe_case(lib, m, d, inter, n_exp, top_k, shared, tag, logits=None):
     sh_gu = F.quantize_matrix(case.gate_up(-1)) if shared else None
     sh_dn = F.quantize_matrix(case.down(-1)) if shared else None
     ref = OM.moe_layer(xf.astype(np.float64), logits, top_k, gate_up, down, sh_gu, sh_dn)
-    return bf16_to_f64(out), ref, (ids, offsets, pairs)
+    return got, ref, (ids, offsets, pairs)
 
 
-@pytest.mark.parametrize("m", [1, 2, 5, 8, 9, 15, 16])
+@pytest.mark.parametrize("m", [1, 2, 5, 8, 9, 15, 16, 17, 33, 64, 100])
 @pytest.mark.parametrize("shared", [True, False])
 def test_moe_small(lib, m, shared):
+    """m <= 16: one segment per expert; m > 16 (prefill): each expert's pairs in
+    blocks of 16, the last one ragged, and the shared expert in blocks of 16 tokens."""
     got, ref, (ids, offsets, pairs) = _moe_case(lib, m, 128, 64, 8, 3, shared, "moe-small")
     assert np.array_equal(ids.cpu().numpy(), ref["ids"])
     assert np.array_equal(offsets.cpu().numpy(), ref["offsets"])
@@ -125,8 +133,41 @@ def test_moe_ragged_and_concentrated(lib):
     check_bound(got, ref["out"], ref["tol_scale"], True, "moe concentrated")
 
 
+def test_moe_prefill_concentrated(lib):
+    """Every one of 40 tokens routed to the same two experts: each gets blocks of 16,
+    16 and 8 pairs, and the shared expert blocks of 16, 16 and 8 tokens."""
+    m, n_exp, top_k = 40, 6, 2
+    logits = np.full((m, n_exp), -5.0, np.float32)
+    logits[:, 2] = 3.0
+    logits[:, 5] = 2.0
+    got, ref, _ = _moe_case(lib, m, 192, 128, n_exp, top_k, True, "moe-conc", logits=logits)
+    assert ref["counts"][2] == m and ref["counts"][5] == m
+    check_bound(got, ref["out"], ref["tol_scale"], True, "moe prefill concentrated")
+    assert lib.device_error() == 0
+
+
 @pytest.mark.parametrize("m", [1, 15])
 def test_moe_config2_full_size(lib, m):
     got, ref, _ = _moe_case(lib, m, W.HIDDEN, W.INTER, W.N_EXPERTS, W.TOP_K, True, "moe")
     check_bound(got, ref["out"], ref["tol_scale"], True, f"moe config2 m={m}")
+    assert lib.device_error() == 0
+
+
+def test_moe_prefill_config4_full_size(lib):
+    """The M=512 prefill chunk through the full-size layer: all 512 tokens run on the
+    GPU; the oracle checks a sample of tokens spread over the chunk (first, last and
+    seeded picks, so that their pairs fall in first, middle and ragged last blocks)."""
+    m = 512
+    rng = np.random.default_rng(W.seed_of("prefill-sample", m))
+    rows = sorted(set([0, 1, m // 2, m - 1] + rng.choice(m, 4, replace=False).tolist()))
+    got, ref, (ids, offsets, pairs) = _moe_case(lib, m, W.HIDDEN, W.INTER, W.N_EXPERTS, W.TOP_K, True, "moe",
+                                                rows=rows)
+    check_bound(got, ref["out"], ref["tol_scale"], True, f"moe prefill m={m} rows={rows}")
+    # the grouping is bit-exact for the whole chunk
+    case = W.MoECase(m=m, d=W.HIDDEN, inter=W.INTER, n_experts=W.N_EXPERTS, top_k=W.TOP_K, tag="moe")
+    oids, _ = OM.route_topk(case.logits(), W.TOP_K)
+    counts, ooffsets, opairs = OM.group_by_expert(oids, W.N_EXPERTS)
+    assert np.array_equal(offsets.cpu().numpy(), ooffsets)
+    assert np.array_equal(pairs.cpu().numpy(), opairs)
+    assert counts.max() > 16          # experts span several 16-pair blocks
     assert lib.device_error() == 0
