@@ -586,18 +586,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       misc[1] = last;
     }
     __syncthreads();
-    if (misc[1] && threadIdx.x < p.m) {
+    if (misc[1] && warp < p.m) {
+      // the last CTA: warp t reduces token t over every CTA's partial, lanes
+      // taking CTAs lane, lane+32, ... (loads in flight together), then shuffles
       __threadfence();
-      const int tok = threadIdx.x;
+      const int tok = warp;
       float v = -INFINITY;
       int rw = 0x7FFFFFFF;
-      for (unsigned b = 0; b < gridDim.x; ++b) {
-        const float ov = __ldcg(p.am_val + static_cast<size_t>(b) * p.m + tok);
-        const int orow = __ldcg(p.am_idx + static_cast<size_t>(b) * p.m + tok);
+      for (unsigned b0 = 0; b0 < gridDim.x; b0 += 128) {
+        float ov[4];
+        int orow[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const unsigned b = b0 + 32 * j + lane;
+          ov[j] = -INFINITY, orow[j] = 0x7FFFFFFF;
+          if (b < gridDim.x) {
+            ov[j] = __ldcg(p.am_val + static_cast<size_t>(b) * p.m + tok);
+            orow[j] = __ldcg(p.am_idx + static_cast<size_t>(b) * p.m + tok);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (better(ov[j], orow[j], v, rw)) v = ov[j], rw = orow[j];
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+        const int orow = __shfl_xor_sync(0xffffffffu, rw, off);
         if (better(ov, orow, v, rw)) v = ov, rw = orow;
       }
-      p.max_logit[tok] = v;
-      p.argmax[tok] = rw;
+      if (lane == 0) p.max_logit[tok] = v, p.argmax[tok] = rw;
     }
   }
 }
