@@ -579,10 +579,13 @@ MoEWorkspace moe_workspace(int m, int top_k, int n_experts, int d, int inter, bo
   MoEWorkspace w;
   w.h = align16(pairs * inter * sizeof(uint16_t));
   w.d = align16(pairs * d * sizeof(float));
-  // gate_up and down share one fixup area: the down launch starts after gate_up ends
-  w.fix = align16(std::max(fixup_bytes(m, sp.s_gu, ceil_div(2 * inter, kGroupRows), sp.n_seg_max),
-                           fixup_bytes(m, sp.s_dn, ceil_div(d, kGroupRows), sp.n_seg_max)));
-  w.total = w.h + w.d + w.fix;
+  // gate_up and down share one fixup area (the down launch starts after gate_up
+  // ends).  It comes first and always holds the arrival counters, so they sit at
+  // the same offset whatever the shape: a zeroed workspace then serves calls of
+  // any shape, each leaving the counters zero.
+  w.fix = align16(std::max({kFixCounterBytes, fixup_bytes(m, sp.s_gu, ceil_div(2 * inter, kGroupRows), sp.n_seg_max),
+                            fixup_bytes(m, sp.s_dn, ceil_div(d, kGroupRows), sp.n_seg_max)}));
+  w.total = w.fix + w.h + w.d;
   return w;
 }
 
@@ -650,8 +653,8 @@ nvfp4_status moe_ffn_grouped(const uint16_t* x, int32_t m, int32_t top_k, const 
   const MoESplits sp = moe_splits(m, top_k, n_exp, d, inter, true);
   const MoEWorkspace wl = moe_workspace(m, top_k, n_exp, d, inter, true);
   uint8_t* base = static_cast<uint8_t*>(ws);
-  uint16_t* h = reinterpret_cast<uint16_t*>(base);
-  float* dpart = reinterpret_cast<float*>(base + wl.h);
+  uint16_t* h = reinterpret_cast<uint16_t*>(base + wl.fix);
+  float* dpart = reinterpret_cast<float*>(base + wl.fix + wl.h);
 
   Job a{};
   a.w = static_cast<const uint8_t*>(gate_up->data);
@@ -666,7 +669,7 @@ nvfp4_status moe_ffn_grouped(const uint16_t* x, int32_t m, int32_t top_k, const 
   a.x_by_pair = 0;
   a.has_shared = shared;
   a.y = h, a.y_ld = inter;
-  set_fixup(&a, base + wl.h + wl.d);
+  set_fixup(&a, base);
   Plan pa;
   if (!make_plan(m, sp.s_gu, a.ng, a.kc, sp.n_seg_max, n_exp, sp.per_run, false, std::max(1, sm_count()), &pa))
     return NVFP4_ERR_SHAPE;
@@ -686,7 +689,7 @@ nvfp4_status moe_ffn_grouped(const uint16_t* x, int32_t m, int32_t top_k, const 
   b.routing_ready = 1;  // the gate+up grid before it waited for the routing
   b.y = nullptr;
   b.yf = dpart, b.yf_ld = d;
-  set_fixup(&b, base + wl.h + wl.d);
+  set_fixup(&b, base);
   Plan pb;
   if (!make_plan(m, sp.s_dn, b.ng, b.kc, sp.n_seg_max, n_exp, sp.per_run, true, std::max(1, sm_count()), &pb))
     return NVFP4_ERR_SHAPE;

@@ -153,6 +153,17 @@ def test_moe_config2_full_size(lib, m):
     assert lib.device_error() == 0
 
 
+def test_moe_workspace_reused_across_shapes(lib):
+    """One workspace serves calls of different m: a 15-token call fills h and the
+    down outputs, then a 1-token call (which splits K and needs zeroed arrival
+    counters) and a 15-token call again must still match the oracle."""
+    _moe_case(lib, 15, W.HIDDEN, W.INTER, W.N_EXPERTS, W.TOP_K, True, "moe")
+    for m in (1, 15):
+        got, ref, _ = _moe_case(lib, m, W.HIDDEN, W.INTER, W.N_EXPERTS, W.TOP_K, True, "moe")
+        check_bound(got, ref["out"], ref["tol_scale"], True, f"moe reused workspace m={m}")
+    assert lib.device_error() == 0
+
+
 def test_moe_prefill_config4_full_size(lib):
     """The M=512 prefill chunk through the full-size layer: all 512 tokens run on the
     GPU; the oracle checks a sample of tokens spread over the chunk (first, last and
