@@ -408,7 +408,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto stream_piece = [&](auto tn_c) {
         constexpr int TN = decltype(tn_c)::value;
         constexpr int kStep = copy_chunks(TN);
-        for (int ch = 0; ch < nch; ch += kStep) {
+        int ch = 0;
+        if constexpr (kStep == 1 && !kMMA) {
+          // CUDA cores (M <= 7, issue-bound): whole chunks two at a time -- both
+          // stages' waits, both chunks, both refills -- halving the per-chunk
+          // wait and refill work.  Only with 4+ stages, so that two stay in flight
+          // while the pair is consumed.  (The tensor-core path measured slower so.)
+          for (; ns >= 4 && ch + 1 < nch; ch += 2) {
+            const int st1 = st + 1 == ns ? 0 : st + 1;
+            const uint32_t ph1 = st + 1 == ns ? ph ^ 1u : ph;
+            if (!mbar_wait_warp(&bar[st], ph)) {
+              failed = true;
+              return;
+            }
+            if (!mbar_wait_warp(&bar[st1], ph1)) {
+              st = st1, ph = ph1;  // the stage that timed out
+              failed = true;
+              return;
+            }
+            core_chunk<MT, TN>(ring_addr + st * kStageBytes, xr, cl, acc);
+#pragma unroll
+            for (int c = 0; c < NA; ++c) xr[c] += kXChunkBytes;
+            core_chunk<MT, TN>(ring_addr + st1 * kStageBytes, xr, cl, acc);
+#pragma unroll
+            for (int c = 0; c < NA; ++c) xr[c] += kXChunkBytes;
+            __syncwarp();
+            if (lane == 0) {
+              fence_proxy_async_smem();  // this warp's reads of both stages before the next copies into them
+              issue_next(st);
+              issue_next(st1);
+            }
+            st = st1 + 1 == ns ? 0 : st1 + 1;
+            ph = st1 + 1 == ns ? ph1 ^ 1u : ph1;
+          }
+        }
+        for (; ch < nch; ch += kStep) {
           if (!mbar_wait_warp(&bar[st], ph)) {
             failed = true;
             return;
