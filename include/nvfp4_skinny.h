@@ -152,7 +152,7 @@ nvfp4_status nvfp4_repack(const uint8_t *nibbles, const uint8_t *scales, int32_t
  *   x   (device) bf16 [m, w->k], 16-byte aligned.
  *   y   (device) bf16 [m, w->n], 4-byte aligned.
  *   ws  (device) nvfp4_gemm_workspace_bytes(m, n, k) bytes, 16-byte aligned.
- *       It holds the k-split fixup area: 256 KiB of arrival counters, then the
+ *       It holds the k-split fixup area: 512 KiB of arrival counters, then the
  *       partial sums.  The counters must be zero before the first call that
  *       uses this workspace (for example cudaMemsetAsync once after
  *       allocation); every completed call leaves them zero again, so the same
@@ -192,7 +192,7 @@ nvfp4_status moe_route_topk(const float *logits, int32_t m, int32_t n_experts, i
  *   shared_gate_up, shared_down: one matrix each of the same shapes, or both NULL.
  *   out             (device) bf16 [m, d].
  *   ws              (device) moe_ffn_workspace_bytes(m, top_k, E, d, inter) bytes,
- *                   16-byte aligned.  It holds a k-split fixup area (256 KiB of
+ *                   16-byte aligned.  It holds a k-split fixup area (512 KiB of
  *                   arrival counters at its start, then partial sums), h and the
  *                   per-(token, slot) down outputs.  The counters must be zero
  *                   before the first call on this workspace (for example
@@ -200,8 +200,9 @@ nvfp4_status moe_route_topk(const float *logits, int32_t m, int32_t n_experts, i
  *                   leaves them zero again, so one workspace of the largest size
  *                   needed serves calls of any shape.
  * Limits: 1 <= m <= 4096, m * top_k <= 16384, d % 64 == 0, inter % 64 == 0.
- * m > 16 is a prefill chunk: each expert's pairs run in blocks of at most 16
- * through the same tensor-core tile as decode, one block after another.
+ * m > 16 is a prefill chunk: each expert's pairs (and the shared expert's
+ * tokens) run in blocks of at most 32, each block's dequantized weight tiles
+ * feeding four 8-slot tensor-core MMA columns.
  */
 size_t moe_ffn_workspace_bytes(int32_t m, int32_t top_k, int32_t n_experts, int32_t d, int32_t inter);
 nvfp4_status moe_ffn_grouped(const uint16_t *x, int32_t m, int32_t top_k, const float *probs,

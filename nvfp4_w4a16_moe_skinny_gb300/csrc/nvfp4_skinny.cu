@@ -86,16 +86,18 @@ bool use_mma(int m) { return m >= 8; }
 // accumulator floats per lane and 16-row tile (the fixup partial of one tile)
 int acc_per_tile(int m) { return use_mma(m) ? (m <= 8 ? 4 : 8) : 2 * m; }
 
-// A fixup area is a fixed 256 KiB of arrival counters (one per segment x group x
-// tile, at most 65,536) followed by the partials.  The counters sit at the same
+// A fixup area is a fixed 512 KiB of arrival counters (one per segment x group x
+// tile, at most 131,072) followed by the partials.  The counters sit at the same
 // place whatever the shape, and every call leaves them zero, so one zero-filled
 // workspace can serve calls of different shapes.
-constexpr size_t kFixCounterBytes = 256 * 1024;
+constexpr size_t kFixCounterBytes = 512 * 1024;
 
+// Partial floats per lane and tile: the decode kernel's accumulator, or the
+// prefill kernel's four 8-slot MMA columns (m > 16).
 size_t fixup_bytes(int m, int S, int ng, int n_seg_max) {
   if (S <= 1) return 0;
   return kFixCounterBytes +
-         static_cast<size_t>(n_seg_max) * ng * 4 * S * 32 * acc_per_tile(std::min(m, 16)) * sizeof(float);
+         static_cast<size_t>(n_seg_max) * ng * 4 * S * 32 * (m > 16 ? 16 : acc_per_tile(m)) * sizeof(float);
 }
 
 // Launch plan for split S on a grid of multiples of `sms` CTAs: one CTA per SM
@@ -109,21 +111,32 @@ size_t fixup_bytes(int m, int S, int ng, int n_seg_max) {
 bool make_plan(int m, int S, int ng, int kc, int n_seg_max, int n_experts, bool per_run, bool x_by_pair, int sms,
                Plan* out) {
   const int L = ceil_div(kc, S);
+  if (per_run) {
+    // the prefill kernel: a run never crosses a slice, so the staged rows (32 and
+    // the zero row) cover one slice; one CTA per SM
+    for (int ns = 8; ns >= 2; --ns) {
+      const size_t smem = prefill_smem_bytes(L, ns, n_seg_max);
+      if (smem <= kMaxSmem) {
+        *out = Plan{S, L, ns, L, kPrefillSlots, 1, sms, n_seg_max, true, smem};
+        return true;
+      }
+    }
+    return false;
+  }
   const int per_seg = S * ng;
   int prev_segs = -1;
   for (int grid = sms;; grid += sms) {
     const long long nu_max = (static_cast<long long>(n_seg_max) * per_seg + grid - 1) / grid;
     const int segs = static_cast<int>(std::min<long long>(n_seg_max, (nu_max + per_seg - 1) / per_seg + 1));
-    if (!per_run && segs > kMaxCtaSegs) continue;
+    if (segs > kMaxCtaSegs) continue;
     int xs_chunks = kc;
-    if (segs == 1 || per_run) {
+    if (segs == 1) {
       const long long nu_seg = std::min<long long>(nu_max, per_seg);  // units of one run
       xs_chunks = static_cast<int>(std::min<long long>(kc, ((nu_seg + ng - 1) / ng + 1) * L));
     }
-    const int xs_rows = per_run ? 16 : (x_by_pair ? segs * std::min(m, 16) : m);
+    const int xs_rows = x_by_pair ? segs * std::min(m, 16) : m;
     for (int ns = 8; ns >= 2; --ns) {
-      const size_t smem = per_run ? prefill_smem_bytes(xs_chunks, ns, n_seg_max)
-                                  : stream_smem_bytes(xs_rows, xs_chunks, ns, n_experts);
+      const size_t smem = stream_smem_bytes(xs_rows, xs_chunks, ns, n_experts);
       if (smem <= kMaxSmem) {
         *out = Plan{S, L, ns, xs_chunks, xs_rows, std::min(segs, kMaxCtaSegs), grid, n_seg_max, per_run, smem};
         return true;
@@ -131,7 +144,7 @@ bool make_plan(int m, int S, int ng, int kc, int n_seg_max, int n_experts, bool 
     }
     // staging the rows of fewer segments per CTA (a larger grid) is the only
     // way left to fit; stop once the grid no longer lowers the count
-    if (!x_by_pair || per_run || segs == prev_segs) return false;
+    if (!x_by_pair || segs == prev_segs) return false;
     prev_segs = segs;
   }
 }
@@ -180,6 +193,16 @@ int choose_split_uncached(int m, int ng, int kc, int n_seg_est, int n_seg_max, i
   int best = 1;
   double best_cost = 1e30;
   Plan pl;
+  if (per_run) {
+    // the prefill kernel: the smallest split whose slice of 32 staged rows fits
+    // (each further split only adds fixup traffic)
+    for (int s = 1; s <= std::min(kMaxSplit, kc); ++s) {
+      if (s > 1 && (!allow_split || static_cast<size_t>(n_seg_max) * ng * 4 > kFixCounterBytes / sizeof(unsigned)))
+        break;
+      if (make_plan(m, s, ng, kc, n_seg_max, n_experts, true, x_by_pair, kPlanSMs, &pl)) return s;
+    }
+    return 1;
+  }
   if (make_plan(m, 1, ng, kc, n_seg_max, n_experts, per_run, x_by_pair, kPlanSMs, &pl))
     best_cost = plan_cost(m, ng, n_seg_est, x_by_pair, pl);
   if (!allow_split) return 1;
@@ -530,26 +553,31 @@ namespace {
 size_t align16(size_t b) { return (b + 15) & ~static_cast<size_t>(15); }
 
 // Segments of a MoE job: each expert that received pairs contributes one
-// segment per block of at most 16 of its pairs (one block when m <= 16), the
-// shared expert one per block of at most 16 tokens.  expected_segments is the
-// planning estimate under uniform routing (each expert's count binomial), and
+// segment per block of its pairs -- one block when m <= 16 (the decode kernel),
+// blocks of at most 32 otherwise (the prefill kernel) -- and the shared expert
+// one per block of tokens of the same size.  expected_segments is the planning
+// estimate under uniform routing (each expert's count binomial), and
 // max_segments the most any routing can produce.
+int segment_block(int m) { return m > 16 ? kPrefillSlots : 16; }
+
 int expected_segments(int m, int top_k, int n_experts, bool shared) {
+  const int blk = segment_block(m);
   const double q = static_cast<double>(top_k) / n_experts;
   double blocks = 0.0, pmf = std::pow(1.0 - q, m);  // P(count = 0)
   for (int c = 1; c <= m; ++c) {
     pmf *= (static_cast<double>(m - c + 1) / c) * (q / (1.0 - q));
-    blocks += pmf * ((c + 15) / 16);
+    blocks += pmf * ((c + blk - 1) / blk);
     if (c > 64 && pmf < 1e-12) break;
   }
   const int est = static_cast<int>(n_experts * blocks + 0.5);
-  return std::max(1, est) + (shared ? (m + 15) / 16 : 0);
+  return std::max(1, est) + (shared ? (m + blk - 1) / blk : 0);
 }
 
 int max_segments(int m, int top_k, int n_experts, bool shared) {
+  const int blk = segment_block(m);
   const int pairs = m * top_k;
-  const int experts = std::min(n_experts, pairs) + (m > 16 ? (pairs + 15) / 16 : 0);
-  return experts + (shared ? (m + 15) / 16 : 0);
+  const int experts = std::min(n_experts, pairs) + (m > 16 ? (pairs + blk - 1) / blk : 0);
+  return experts + (shared ? (m + blk - 1) / blk : 0);
 }
 
 struct MoESplits {

@@ -3,30 +3,33 @@
 // The same contraction as the decode path (TensorSharp docs/models/gemma4.md,
 // "14. Optimization opportunities / Completed": expert-batched gate+up and down
 // over the tokens routed to each expert), when an expert may receive more than
-// 16 pairs.  Each expert's pairs are cut into blocks of at most 16, and each
-// block is a *segment* that runs through the M <= 16 tensor-core tile (16x64
-// NVFP4 weight tiles dequantized to f16 against the block's 16 activation rows,
-// mma.sync m16n8k16, fp32 accumulation); the shared expert is cut the same way
-// into blocks of 16 tokens.
+// 16 pairs.  Each expert's pairs are cut into blocks of at most 32, and each
+// block is a *segment* of 32 token slots: every dequantized 16x64 NVFP4 weight
+// tile feeds four 8-slot m16n8k16 MMA columns (f16 in, fp32 accumulation), so an
+// expert's weights are streamed and dequantized once per 32 pairs.  The shared
+// expert is cut the same way into blocks of 32 tokens.
 //
-// Work decomposition.  As in the decode kernel: a unit is (segment, K slice,
-// 64-row group), units are numbered segment-major and dealt to the grid in
-// contiguous balanced ranges, and a warp's share of a unit (a piece, 1-4 tiles)
-// streams through the warp's own ring of TMA / bulk copies.  A CTA's range may
-// cross several segments, each with its own 16 activation rows, so the CTA walks
-// its range one segment at a time (a *run*): it stages the run's rows, deals the
-// run's units to its warps, and moves to the next run once every warp is done.
-// The weight copies run ahead across runs; only the staging waits.
+// Work decomposition.  A unit is (segment, K slice, 64-row group, half): two
+// 16-row tiles.  Units are numbered segment-major, then slice, group and half,
+// and dealt to the grid in contiguous balanced ranges; a warp's share of a unit
+// (a piece, 1-2 tiles) streams through the warp's own ring of TMA boxes.  A
+// CTA's range crosses (segment, slice) blocks, each with its own 32 activation
+// rows over its own columns, so the CTA walks its range one block at a time (a
+// *run*): it stages the run's rows, deals the run's units to its warps, and
+// moves on once every warp is done.  The weight copies run ahead across runs;
+// only the staging waits.  Runs never span slices, so the staged rows cover one
+// slice and K may be split (S > 1, with the decode path's fixup) when a slice
+// of 32 rows of the whole K would not fit beside the rings.
 #pragma once
 
 #include "kernel.cuh"
 
 namespace nvfp4 {
 
-constexpr int kPrefillSlots = 16;  // activation rows of one segment
+constexpr int kPrefillSlots = 32;  // activation rows of one segment (four 8-slot MMA columns)
 
-// Tables after the staged rows (4-byte entries): row_src[16], sigma[17],
-// slot_row[16], slot_out[16], mul[16], the warps' copy cursors [16 x 8], the
+// Tables after the staged rows (4-byte entries): row_src[32], sigma[33],
+// slot_row[32], slot_out[32], mul[32], the warps' copy cursors [16 x 8], the
 // segment list and the block of each segment [max_segs + 1 each], misc[4].
 constexpr int kPrefillFixedEntries = 5 * kPrefillSlots + 1 + kWarps * 8;
 
@@ -45,7 +48,7 @@ template <int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ Job p, const __grid_constant__ WeightMaps maps) {
   static_assert(kEpi == kEpiGated || kEpi == kEpiRows, "grouped products only");
-  constexpr int NT = 2;       // two 8-slot MMA columns: a segment's 16 slots
+  constexpr int NT = 4;       // four 8-slot MMA columns: a segment's 32 slots
   constexpr int NI = 4;       // floats per accumulator column
   constexpr int V = NT * NI;  // accumulator floats per lane and tile
   extern __shared__ __align__(128) uint8_t smem[];
@@ -59,14 +62,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + ring_bytes) + warp * ns;
   uint8_t* xs = smem + ring_bytes + static_cast<size_t>(kWarps) * ns * 8;
   const size_t xs_bytes = static_cast<size_t>(kPrefillSlots + 1) * (static_cast<size_t>(p.xs_chunks) * kXChunkBytes + 16);
-  int* row_src = reinterpret_cast<int*>(xs + xs_bytes);  // [16] source row of each staged row
-  int* sigma = row_src + kPrefillSlots;                   // [17] power-of-two scale of each staged row
-  int* slot_row = sigma + kPrefillSlots + 1;              // [16] staged row of each slot
-  int* slot_out = slot_row + kPrefillSlots;               // [16] output row of each slot, -1: none
-  float* mul = reinterpret_cast<float*>(slot_out + kPrefillSlots);  // [16] global scale of the segment
+  int* row_src = reinterpret_cast<int*>(xs + xs_bytes);  // [32] source row of each staged row
+  int* sigma = row_src + kPrefillSlots;                   // [33] power-of-two scale of each staged row
+  int* slot_row = sigma + kPrefillSlots + 1;              // [32] staged row of each slot
+  int* slot_out = slot_row + kPrefillSlots;               // [32] output row of each slot, -1: none
+  float* mul = reinterpret_cast<float*>(slot_out + kPrefillSlots);  // [32] global scale of the segment
   int* cur = reinterpret_cast<int*>(mul + kPrefillSlots) + warp * 8;  // this warp's copy cursor
   int* seg_list = reinterpret_cast<int*>(mul + kPrefillSlots) + kWarps * 8;  // [max_segs + 1] matrix
-  int* seg_blk = seg_list + p.max_segs + 1;  // [max_segs + 1] block: pairs 16b .. 16b+15 of the matrix
+  int* seg_blk = seg_list + p.max_segs + 1;  // [max_segs + 1] block: pairs 32b .. 32b+31 of the matrix
   int* misc = seg_blk + p.max_segs + 1;      // [0] segments, [1] staged rows
   if ((smem_addr(smem) & 127u) || smem_addr(misc + 4) - smem_addr(smem) > dynamic_smem_bytes()) {
     // the carve-up does not fit the launch's shared memory (a plan error): touch nothing
@@ -80,8 +83,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
 
-  // ---- segments: each expert's blocks of at most 16 pairs, then the shared
-  // expert's blocks of at most 16 tokens
+  // ---- segments: each expert's blocks of at most 32 pairs, then the shared
+  // expert's blocks of at most 32 tokens
   if (!p.routing_ready) pdl_wait();
   if (warp == 0) {
     int n = 0;
@@ -110,33 +113,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   const int n_seg = misc[0];
-  const int per_seg = p.S * p.ng;  // units per segment
+  const int upg = 2 * p.ng;         // units of one (segment, slice): two per 64-row group
+  const int per_seg = p.S * upg;    // units per segment
   const long long n_units = static_cast<long long>(n_seg) * per_seg;
   const int u0 = static_cast<int>(n_units * blockIdx.x / gridDim.x);
   const int u1 = static_cast<int>(n_units * (blockIdx.x + 1) / gridDim.x);
-  const int cseg0 = u1 > u0 ? u0 / per_seg : 0;                      // this CTA's first segment
-  const int nsc = u1 > u0 ? (u1 - 1) / per_seg - cseg0 + 1 : 0;      // segments (runs) it touches
-  // run r: the CTA's units of segment cseg0 + r, and the K chunks [c_lo, c_hi)
-  // they touch (their slices; the whole of K once the run spans all slices)
-  auto run_lo = [&](int r) { return max(u0, (cseg0 + r) * per_seg); };
-  auto run_hi = [&](int r) { return min(u1, (cseg0 + r + 1) * per_seg); };
-  auto col_span = [&](int r, int& c_lo, int& c_hi) {
-    const int sb = (cseg0 + r) * per_seg;
-    c_lo = ((run_lo(r) - sb) / p.ng) * p.L;
-    c_hi = min(p.kc, ((run_hi(r) - 1 - sb) / p.ng + 1) * p.L);
-  };
-  bool fits = true;
-  for (int r = 0; r < nsc && fits; ++r) {
-    int a, b;
-    col_span(r, a, b);
-    fits = b - a <= p.xs_chunks;
-  }
-  if (!fits && threadIdx.x == 0) atomicOr(&g_device_error, kErrPlan);  // the plan does not cover this CTA
-  const int n_runs = fits ? nsc : 0;
+  // run r: the CTA's units of (segment, slice) block b0 + r; its activation rows
+  // are the segment's, over the slice's columns
+  const int b0 = u1 > u0 ? u0 / upg : 0;
+  const int n_blk = u1 > u0 ? (u1 - 1) / upg - b0 + 1 : 0;
+  auto run_lo = [&](int r) { return max(u0, (b0 + r) * upg); };
+  auto run_hi = [&](int r) { return min(u1, (b0 + r + 1) * upg); };
+  auto run_seg = [&](int r) { return (b0 + r) / p.S; };
+  auto run_slice = [&](int r) { return (b0 + r) - run_seg(r) * p.S; };
+  const bool fits = p.L <= p.xs_chunks;
+  if (!fits && threadIdx.x == 0) atomicOr(&g_device_error, kErrPlan);  // the plan does not cover a slice
+  const int n_runs = fits ? n_blk : 0;
 
-  // ---- warp w's pieces of run r: whole units round-robin (warp w takes units w,
-  // w+16, ...), or the units' tiles as contiguous ranges, whichever leaves the
-  // busiest warp less work
+  // ---- warp w's pieces of run r: whole units (2 tiles) round-robin (warp w takes
+  // units w, w+16, ...), or the units' tiles as contiguous ranges, whichever
+  // leaves the busiest warp less work
   struct Deal {
     int lo, nu, T0, T1, np;
     bool whole;
@@ -145,41 +141,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     Deal d;
     d.lo = run_lo(r);
     d.nu = run_hi(r) - d.lo;
-    d.whole = deal_whole(d.nu);
-    d.T0 = (4 * d.nu * warp) / kWarps, d.T1 = (4 * d.nu * (warp + 1)) / kWarps;
-    d.np = d.whole ? (d.nu - warp + kWarps - 1) / kWarps : (d.T1 > d.T0 ? ((d.T1 - 1) >> 2) - (d.T0 >> 2) + 1 : 0);
+    d.whole = (d.nu + kWarps - 1) / kWarps * 2 * 100 <= (2 * d.nu + kWarps - 1) / kWarps * 115;
+    d.T0 = (2 * d.nu * warp) / kWarps, d.T1 = (2 * d.nu * (warp + 1)) / kWarps;
+    d.np = d.whole ? (d.nu - warp + kWarps - 1) / kWarps : (d.T1 > d.T0 ? ((d.T1 - 1) >> 1) - (d.T0 >> 1) + 1 : 0);
     return d;
   };
   struct Piece {
-    int seg, s, grp, t0, tn;
+    int seg, s, grp, t0, tn;  // t0: first tile (0..3) of the group
   };
   auto piece_at = [&](const Deal& d, int k) -> Piece {
     int unit, t0, tn;
     if (d.whole) {
-      unit = d.lo + k * kWarps + warp, t0 = 0, tn = 4;
+      unit = d.lo + k * kWarps + warp, t0 = 0, tn = 2;
     } else {
-      const int start = k == 0 ? d.T0 : ((d.T0 >> 2) + k) << 2;
-      const int end = min(d.T1, ((d.T0 >> 2) + k + 1) << 2);
-      unit = d.lo + (start >> 2), t0 = start & 3, tn = end - start;
+      const int start = k == 0 ? d.T0 : ((d.T0 >> 1) + k) << 1;
+      const int end = min(d.T1, ((d.T0 >> 1) + k + 1) << 1);
+      unit = d.lo + (start >> 1), t0 = start & 1, tn = end - start;
     }
     Piece pc;
     pc.seg = unit / per_seg;
     const int r = unit - pc.seg * per_seg;
-    pc.s = r / p.ng;
-    pc.grp = r - pc.s * p.ng;
-    pc.t0 = t0, pc.tn = tn;
+    pc.s = r / upg;
+    const int q = r - pc.s * upg;  // 2 * group + half
+    pc.grp = q >> 1;
+    pc.t0 = 2 * (q & 1) + t0, pc.tn = tn;
     return pc;
   };
   auto slice_len = [&](int s) { return min(p.kc, (s + 1) * p.L) - s * p.L; };
 
   // ---- producer (lane 0): cursor over this warp's pieces, run after run, ahead
-  // of the consumer by the ring's depth.  A whole unit is one 2,304-byte bulk
-  // copy per chunk; a piece of 1-3 tiles is TMA boxes of copy_chunks(tn) chunks.
-  // Cursor (lane 0's, in shared memory): [0] map index (tn-1, +4 for the shared
-  // expert), [1] first tile, [2] next chunk, [3] group, [4] chunks per copy,
-  // [5] run, [6] next piece of the run.
-  int prem = 0;                   // copies left in the open piece
-  const uint8_t* psrc = nullptr;  // next bulk-copy source; nullptr: TMA boxes
+  // of the consumer by the ring's depth.  A piece of tn tiles is TMA boxes of tn
+  // tiles x copy_chunks(tn) chunks (2,304 bytes each).  Cursor (lane 0's, in
+  // shared memory): [0] map index (tn-1, +4 for the shared expert), [1] first
+  // tile, [2] next chunk, [3] group, [4] chunks per copy, [5] run, [6] next piece.
+  int prem = 0;  // copies left in the open piece
   const uint64_t policy = l2_evict_first_policy();
   uint8_t* ring = smem + static_cast<size_t>(warp) * ns * kStageBytes;
   const uint32_t ring_s = smem_addr(ring), bar_s = smem_addr(bar);
@@ -195,38 +190,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const Piece pc = piece_at(d, cur[6]++);
       const int e = seg_list[pc.seg];
-      const int group = (e >= 0 ? e * p.ng : 0) + pc.grp;  // within the stack
-      if (pc.tn == kChunkTiles) {
-        prem = slice_len(pc.s);
-        psrc = (e == kSharedSeg ? p.w_sh : p.w) + (static_cast<size_t>(group) * p.kc + pc.s * p.L) * kStageBytes;
-      } else {
-        const int step = copy_chunks(pc.tn);
-        prem = (slice_len(pc.s) + step - 1) / step;
-        psrc = nullptr;
-        cur[0] = (pc.tn - 1) + (e == kSharedSeg ? 4 : 0);
-        cur[1] = pc.t0;
-        cur[2] = pc.s * p.L;
-        cur[3] = group;
-        cur[4] = step;
-      }
+      const int step = copy_chunks(pc.tn);
+      prem = (slice_len(pc.s) + step - 1) / step;
+      cur[0] = (pc.tn - 1) + (e == kSharedSeg ? 4 : 0);
+      cur[1] = pc.t0;
+      cur[2] = pc.s * p.L;
+      cur[3] = (e >= 0 ? e * p.ng : 0) + pc.grp;  // group within the stack
+      cur[4] = step;
     }
-    const uint32_t b = bar_s + stage * 8, dst = ring_s + stage * kStageBytes;
-    if (psrc) {
-      mbar_arrive_expect_tx_s(b, kStageBytes);
-      bulk_g2s_s(dst, psrc, kStageBytes, b, policy);
-      psrc += kStageBytes;
-    } else {
-      const int mi = cur[0];
-      mbar_arrive_expect_tx_s(b, static_cast<uint32_t>(((mi & 3) + 1) * cur[4]) * kTileBytes);
-      tma_load_4d_s(dst, mi < 4 ? &maps.w[mi] : &maps.sh[mi - 4], 0, cur[1], cur[2], cur[3], b, policy);
-      cur[2] += cur[4];
-    }
+    const int mi = cur[0];
+    const uint32_t b = bar_s + stage * 8;
+    mbar_arrive_expect_tx_s(b, static_cast<uint32_t>(((mi & 3) + 1) * cur[4]) * kTileBytes);
+    tma_load_4d_s(ring_s + stage * kStageBytes, mi < 4 ? &maps.w[mi] : &maps.sh[mi - 4], 0, cur[1], cur[2], cur[3], b,
+                  policy);
+    cur[2] += cur[4];
     --prem;
   };
   if (lane == 0)
     for (int st = 0; st < ns; ++st) issue_next(st);
 
-  // ---- run r's tables (thread j < 16: slot j of the segment): the source row
+  // ---- run r's tables (thread j < 32: slot j of the segment): the source row
   // it stages (gate+up: the pair's token row of x; down: the pair's gate+up
   // output row), its output row, and the segment's global scale.  Empty slots
   // read the zero row (index = valid slots) and write nothing.  The down
@@ -235,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto build_tables = [&](int r) {
     if (threadIdx.x < kPrefillSlots && n_runs > 0) {
       const int j = threadIdx.x;
-      const int e = seg_list[cseg0 + r], b = seg_blk[cseg0 + r];
+      const int e = seg_list[run_seg(r)], b = seg_blk[run_seg(r)];
       const int cnt = e == kSharedSeg ? p.m : __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
       const int v = min(kPrefillSlots, cnt - kPrefillSlots * b);  // valid slots (>= 1)
       int out = -1;
@@ -254,13 +237,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j == 0) misc[1] = v;
     }
   };
-  int c_lo = 0, c_hi = 0, stride = 16, nrows = 0;
-  // after build_tables(r) and a barrier: stage run r's rows (ends with a barrier)
+  int c_lo = 0, stride = 16, nrows = 0;
+  // after build_tables(r) and a barrier: stage run r's rows over its slice's
+  // columns (ends with a barrier)
   auto stage_run = [&](int r) {
-    if (n_runs > 0) col_span(r, c_lo, c_hi);
-    stride = (c_hi - c_lo) * kXChunkBytes + 16;
+    const int nch = n_runs > 0 ? slice_len(run_slice(r)) : 0;
+    c_lo = n_runs > 0 ? run_slice(r) * p.L : 0;
+    stride = nch * kXChunkBytes + 16;
     nrows = n_runs > 0 ? misc[1] : 0;
-    stage_rows<true>(p.x, p.k, c_lo * kTileK, c_hi - c_lo, nrows, row_src, sigma, xs, stride);
+    stage_rows<true>(p.x, p.k, c_lo * kTileK, nch, nrows, row_src, sigma, xs, stride);
   };
   if (p.routing_ready) {
     build_tables(0);
@@ -272,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   stage_run(0);
 
   const uint32_t xs_addr = smem_addr(xs);
-  float acc[4][NT][NI];
+  float acc[2][NT][NI];
 
   // Finish tile t (0..3) of group grp from a[] (output units).  MMA fragment:
   // column c holds slots c*8 + 2*t4 + (i & 1) of rows g (i < 2) and g + 8.
@@ -299,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool failed = false;  // a copy did not complete in time
   for (int r = 0; r < n_runs; ++r) {
     if (r > 0) {
-      // the next segment's rows replace the staged ones once every warp is done
+      // the next run's rows replace the staged ones once every warp is done
       __syncthreads();
       build_tables(r);
       __syncthreads();
@@ -308,19 +293,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Deal d = deal_of(r);
     for (int k = 0; k < d.np && !failed; ++k) {
       const Piece pc = piece_at(d, k);
-      const int kc0 = pc.s * p.L, nch = slice_len(pc.s);
-      const uint32_t xbase = xs_addr + (kc0 - c_lo) * kXChunkBytes;
+      const int nch = slice_len(pc.s);
       uint32_t xr[NT];
 #pragma unroll
-      for (int c = 0; c < NT; ++c) xr[c] = xbase + slot_row[c * 8 + g] * stride + t4 * 32;
+      for (int c = 0; c < NT; ++c) xr[c] = xs_addr + slot_row[c * 8 + g] * stride + t4 * 32;
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < 2; ++a)
 #pragma unroll
         for (int c = 0; c < NT; ++c)
 #pragma unroll
           for (int i = 0; i < NI; ++i) acc[a][c][i] = 0.f;
-      // the piece's copies: copy j holds chunks j*step .. of the slice, each TN
-      // tiles at stage + c*TN*576 (one loop per TN, chosen once per piece)
+      // the piece's copies: copy j holds chunks j*step .. of the slice, TN tiles
+      // each at stage + cc*TN*576
       auto stream_piece = [&](auto tn_c) {
         constexpr int TN = decltype(tn_c)::value;
         constexpr int kStep = copy_chunks(TN);
@@ -344,12 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++st == ns) st = 0, ph ^= 1u;
         }
       };
-      switch (pc.tn) {
-        case 4: stream_piece(std::integral_constant<int, 4>{}); break;
-        case 3: stream_piece(std::integral_constant<int, 3>{}); break;
-        case 2: stream_piece(std::integral_constant<int, 2>{}); break;
-        default: stream_piece(std::integral_constant<int, 1>{}); break;
-      }
+      if (pc.tn == 2)
+        stream_piece(std::integral_constant<int, 2>{});
+      else
+        stream_piece(std::integral_constant<int, 1>{});
       if (failed) break;
       // ---- to output units: times g * 2^(8 - sigma of the slot's staged row)
       float mulv[NT][2];
@@ -362,21 +344,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           mulv[c][h] = row < nrows ? mul[slot] * exp2i(8 - sigma[row]) : 0.f;
         }
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < 2; ++a)
 #pragma unroll
         for (int c = 0; c < NT; ++c)
 #pragma unroll
           for (int i = 0; i < NI; ++i) acc[a][c][i] *= mulv[c][i & 1];
       if (p.S == 1) {
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
+        for (int a = 0; a < 2; ++a)
           if (a < pc.tn) finish_tile(pc.grp, pc.t0 + a, acc[a]);
       } else {
         // ---- k-split: per tile, store the partial and take a ticket; the last of
         // the S slices sums all S partials in slice order and finishes the tile
         const size_t cell0 = (static_cast<size_t>(pc.seg) * p.ng + pc.grp) * 4 + pc.t0;
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
+        for (int a = 0; a < 2; ++a) {
           if (a >= pc.tn) break;
           float* dst = p.fix + (((cell0 + a) * p.S + pc.s) * 32 + lane) * V;
 #pragma unroll
@@ -388,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned last = 0;  // bit a: this warp completed tile t0 + a
         if (lane == 0) {
 #pragma unroll
-          for (int a = 0; a < 4; ++a)
+          for (int a = 0; a < 2; ++a)
             if (a < pc.tn && atomicAdd(&p.fix_cnt[cell0 + a], 1u) == static_cast<unsigned>(p.S - 1)) {
               last |= 1u << a;
               atomicExch(&p.fix_cnt[cell0 + a], 0u);
@@ -397,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) __threadfence();
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
+        for (int a = 0; a < 2; ++a) {
           if (!((last >> a) & 1u)) continue;
           float sum[NT][NI];
 #pragma unroll

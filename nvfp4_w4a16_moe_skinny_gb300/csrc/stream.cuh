@@ -57,9 +57,10 @@ __device__ __forceinline__ void mma_step(uint32_t word, uint32_t s, const uint32
 // TN tiles at shared address `st` against x fragments at xr[nt] (this lane's 32
 // bytes of slot 8*nt + g for the chunk).  acc[r][nt] is tile r's C fragment:
 // [0],[1] = row g, slots 8nt+2t, +1; [2],[3] = row g+8.
-template <int NT, int TN>
+template <int NT, int TN, int NR>
 __device__ __forceinline__ void mma_chunk(uint32_t st, const uint32_t (&xr)[NT], int lane,
-                                          float (&acc)[4][NT][4]) {
+                                          float (&acc)[NR][NT][4]) {
+  static_assert(TN <= NR, "one accumulator per tile");
   uint4 xa[NT], xb[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {

@@ -66,8 +66,8 @@ def test_sizes_reject_bad_shapes(so):
     assert so.moe_ffn_workspace_bytes(512, 8, 128, 2816, 704) >= (512 * 8 + 512) * (704 * 2 + 2816 * 4)
     # h (bf16) and the per-(token, slot) down outputs (fp32) are always part of it
     assert so.moe_ffn_workspace_bytes(15, 8, 128, 2816, 704) >= (15 * 8 + 15) * (704 * 2 + 2816 * 4)
-    # the fixed 256 KiB counter area leads every MoE workspace, whatever the split
-    assert so.moe_ffn_workspace_bytes(1, 1, 8, 64, 64) >= 256 * 1024 + 2 * (64 * 2 + 64 * 4)
+    # the fixed 512 KiB counter area leads every MoE workspace, whatever the split
+    assert so.moe_ffn_workspace_bytes(1, 1, 8, 64, 64) >= 512 * 1024 + 2 * (64 * 2 + 64 * 4)
 
 
 def _weight(data=1 << 20, gs=1 << 20, n=64, k=64, e=1, flags=0, version=2):

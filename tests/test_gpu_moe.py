@@ -114,7 +114,7 @@ def _moe_case(lib, m, d, inter, n_exp, top_k, shared, tag, logits=None, rows=Non
 @pytest.mark.parametrize("shared", [True, False])
 def test_moe_small(lib, m, shared):
     """m <= 16: one segment per expert; m > 16 (prefill): each expert's pairs in
-    blocks of 16, the last one ragged, and the shared expert in blocks of 16 tokens."""
+    blocks of 32, the last one ragged, and the shared expert in blocks of 32 tokens."""
     got, ref, (ids, offsets, pairs) = _moe_case(lib, m, 128, 64, 8, 3, shared, "moe-small")
     assert np.array_equal(ids.cpu().numpy(), ref["ids"])
     assert np.array_equal(offsets.cpu().numpy(), ref["offsets"])
@@ -134,8 +134,8 @@ def test_moe_ragged_and_concentrated(lib):
 
 
 def test_moe_prefill_concentrated(lib):
-    """Every one of 40 tokens routed to the same two experts: each gets blocks of 16,
-    16 and 8 pairs, and the shared expert blocks of 16, 16 and 8 tokens."""
+    """Every one of 40 tokens routed to the same two experts: each gets blocks of 32
+    and 8 pairs, and the shared expert blocks of 32 and 8 tokens."""
     m, n_exp, top_k = 40, 6, 2
     logits = np.full((m, n_exp), -5.0, np.float32)
     logits[:, 2] = 3.0
