@@ -19,28 +19,21 @@ namespace nvfp4 {
 
 // ------------------------------------------------------------------ router
 
-// One CTA.  Phase 1: one warp per token selects the top_k largest logits
-// (descending, ties -> lower expert id) by repeated warp arg-max and takes a
-// softmax over them; lane r keeps the r-th choice.  Phase 2: a stable counting
-// sort of the (token, slot) pairs by expert with warp ballots: counts, a
-// block-wide exclusive scan, then ranked writes in ascending pair order.  No
-// atomics.  NPER: logits per lane (n_experts <= 32 * NPER).
+// Phase 1: one warp per token selects the top_k largest logits (descending,
+// ties -> lower expert id) by repeated warp arg-max and takes a softmax over
+// them; lane r keeps the r-th choice.  Phase 2: a stable counting sort of the
+// (token, slot) pairs by expert: counts, a block-wide exclusive scan, then
+// ranked writes in ascending pair order.  No atomics.  A decode batch (m <= 32)
+// runs both phases in one CTA; a larger batch runs phase 1 over many CTAs and
+// phase 2 in one.  NPER: logits per lane (n_experts <= 32 * NPER).
 constexpr int kRouteThreads = 1024;
 
+// Top-k + softmax of token t by one warp; lane r < top_k writes the r-th choice
+// (and, when s_ids is given, also into shared memory).
 template <int NPER>
-__global__ void __launch_bounds__(kRouteThreads, 1)
-    moe_route_kernel(const float* __restrict__ logits, int m, int n_experts, int top_k, int* __restrict__ ids,
-                     float* __restrict__ probs, int* __restrict__ offsets, int* __restrict__ sorted_pairs) {
-  extern __shared__ int route_smem[];
-  const int pairs = m * top_k;
-  int* s_ids = route_smem;                 // [pairs]
-  int* s_cnt = s_ids + pairs;              // [n_experts + 1]
-  int* s_wsum = s_cnt + n_experts + 1;     // [32] per-warp totals of the scan
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
-  pdl_wait();  // the logits may come from the previous grid
-  pdl_launch_dependents();
-  for (int t = warp; t < m; t += nwarps) {
+__device__ __forceinline__ void token_topk(const float* __restrict__ logits, int t, int n_experts, int top_k, int lane,
+                                           int* __restrict__ ids, float* __restrict__ probs, int* s_ids) {
+  {
     const float* row = logits + static_cast<size_t>(t) * n_experts;
     float lv[NPER];  // experts lane + 32*i, read once
 #pragma unroll
@@ -77,10 +70,17 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     if (lane < top_k) {
       ids[t * top_k + lane] = mye;
       probs[t * top_k + lane] = ez / z;
-      s_ids[t * top_k + lane] = mye;
+      if (s_ids) s_ids[t * top_k + lane] = mye;
     }
   }
-  __syncthreads();
+}
+
+// The stable counting sort of the pairs by expert, from s_ids[pairs] in shared
+// memory, by the whole CTA; s_cnt[n_experts + 1] and s_wsum[32] are scratch.
+__device__ __forceinline__ void group_pairs(const int* s_ids, int pairs, int n_experts, int* s_cnt, int* s_wsum,
+                                            int* __restrict__ offsets, int* __restrict__ sorted_pairs) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
   // counts per expert (warp per expert, ballots over the pairs)
   for (int e = warp; e < n_experts; e += nwarps) {
     int cnt = 0;
@@ -130,6 +130,127 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
       pos += __popc(mask);
     }
   }
+}
+
+// The same sort for n_experts <= kHistExperts, in three passes over per-warp
+// histograms (hist[w * n_experts + e], scratch of 32 * n_experts ints): warp w
+// owns the contiguous pairs [w*C, (w+1)*C); (1) it counts its pairs per expert,
+// lanes holding the same expert finding each other with a match; (2) thread e
+// turns the counts into the first position of (expert e, warp w) -- expert-major,
+// then warp, which is ascending pair order within an expert; (3) each warp walks
+// its pairs again and places them.  No atomics; every count and position has a
+// single writer.
+constexpr int kHistExperts = 256;
+// Shared-memory ints of the grouping's count scratch.
+__host__ __device__ inline int route_scratch(int n_experts) {
+  return n_experts <= kHistExperts ? 32 * n_experts : n_experts + 1;
+}
+__device__ __forceinline__ void group_pairs_hist(const int* s_ids, int pairs, int n_experts, int* hist, int* s_wsum,
+                                                 int* __restrict__ offsets, int* __restrict__ sorted_pairs) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;  // 32
+  const int per = (pairs + nwarps - 1) / nwarps;
+  const int q0 = min(pairs, warp * per), q1 = min(pairs, q0 + per);
+  for (int i = threadIdx.x; i < nwarps * n_experts; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  int* h = hist + warp * n_experts;
+  for (int base = q0; base < q1; base += 32) {
+    const int q = base + lane;
+    const int e = q < q1 ? s_ids[q] : -1 - lane;  // a lane past the end matches nobody
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    if (q < q1 && lane == __ffs(same) - 1) h[e] += __popc(same);
+    __syncwarp();
+  }
+  __syncthreads();
+  // totals per expert, their exclusive scan (threads = experts), then the first
+  // position of each (expert, warp)
+  const int t = threadIdx.x;
+  int total = 0;
+  if (t < n_experts)
+    for (int w = 0; w < nwarps; ++w) total += hist[w * n_experts + t];
+  int incl = total;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  int excl = incl - total;
+  for (int w = 0; w < warp; ++w) excl += s_wsum[w];
+  if (t < n_experts) {
+    offsets[t] = excl;
+    int run = excl;
+    for (int w = 0; w < nwarps; ++w) {
+      const int c = hist[w * n_experts + t];
+      hist[w * n_experts + t] = run;
+      run += c;
+    }
+  }
+  if (t == 0) offsets[n_experts] = pairs;
+  __syncthreads();
+  for (int base = q0; base < q1; base += 32) {
+    const int q = base + lane;
+    const int e = q < q1 ? s_ids[q] : -1 - lane;
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    if (q < q1) sorted_pairs[h[e] + __popc(same & ((1u << lane) - 1u))] = q;
+    __syncwarp();
+    if (q < q1 && lane == __ffs(same) - 1) h[e] += __popc(same);
+    __syncwarp();
+  }
+}
+
+// A decode batch: one CTA does both (one warp per token, then the grouping).
+template <int NPER>
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    moe_route_kernel(const float* __restrict__ logits, int m, int n_experts, int top_k, int* __restrict__ ids,
+                     float* __restrict__ probs, int* __restrict__ offsets, int* __restrict__ sorted_pairs) {
+  extern __shared__ int route_smem[];
+  const int pairs = m * top_k;
+  int* s_ids = route_smem;                                  // [pairs]
+  int* s_cnt = s_ids + pairs;                               // [route_scratch(n_experts)]
+  int* s_wsum = s_cnt + route_scratch(n_experts);           // [32] per-warp totals of the scan
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  pdl_wait();  // the logits may come from the previous grid
+  pdl_launch_dependents();
+  for (int t = warp; t < m; t += nwarps) token_topk<NPER>(logits, t, n_experts, top_k, lane, ids, probs, s_ids);
+  __syncthreads();
+  // (at most 32 tokens: the ballot sort; the histogram passes cost more here)
+  group_pairs(s_ids, pairs, n_experts, s_cnt, s_wsum, offsets, sorted_pairs);
+}
+
+// A prefill chunk, step 1: the top-k of every token, one warp per token over
+// many CTAs.
+constexpr int kTopkWarps = 8;
+template <int NPER>
+__global__ void __launch_bounds__(kTopkWarps * 32)
+    moe_topk_kernel(const float* __restrict__ logits, int m, int n_experts, int top_k, int* __restrict__ ids,
+                    float* __restrict__ probs) {
+  const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
+  pdl_wait();  // the logits may come from the previous grid
+  pdl_launch_dependents();
+  if (t < m) token_topk<NPER>(logits, t, n_experts, top_k, threadIdx.x & 31, ids, probs, nullptr);
+}
+
+// A prefill chunk, step 2: the grouping of all pairs by one CTA (the histogram
+// sort when the experts allow it: the ballot sort scans every pair once per
+// expert, ~4x slower at 4,096 pairs).
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    moe_group_kernel(const int* __restrict__ ids, int pairs, int n_experts, int* __restrict__ offsets,
+                     int* __restrict__ sorted_pairs) {
+  extern __shared__ int route_smem[];
+  int* s_ids = route_smem;                         // [pairs]
+  int* s_cnt = s_ids + pairs;                      // [route_scratch(n_experts)]
+  int* s_wsum = s_cnt + route_scratch(n_experts);  // [32]
+  pdl_wait();  // the ids come from the previous grid
+  pdl_launch_dependents();
+  for (int q = threadIdx.x; q < pairs; q += blockDim.x) s_ids[q] = __ldg(ids + q);
+  __syncthreads();
+  if (n_experts <= kHistExperts)
+    group_pairs_hist(s_ids, pairs, n_experts, s_cnt, s_wsum, offsets, sorted_pairs);
+  else
+    group_pairs(s_ids, pairs, n_experts, s_cnt, s_wsum, offsets, sorted_pairs);
 }
 
 // out[t, j] = bf16( sum_r probs[t, r] * d[t*top_k + r, j] + d[m*top_k + t, j] ), fixed order.

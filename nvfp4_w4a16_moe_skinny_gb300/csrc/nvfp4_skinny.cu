@@ -631,21 +631,34 @@ nvfp4_status moe_route_topk(const float* logits, int32_t m, int32_t n_experts, i
   if (!aligned(logits, 4) || !aligned(ids, 4) || !aligned(probs, 4) || !aligned(expert_offsets, 4) ||
       !aligned(sorted_pairs, 4))
     return NVFP4_ERR_ALIGN;
-  const size_t smem = sizeof(int) * (static_cast<size_t>(m) * top_k + n_experts + 1 + 32);
+  const size_t smem = sizeof(int) * (static_cast<size_t>(m) * top_k + route_scratch(n_experts) + 32);
   const int nper = ceil_div(n_experts, 32);
-  auto launch = [&](auto kernel) -> nvfp4_status {
-    if (set_smem(kernel, smem) != cudaSuccess) return NVFP4_ERR_CUDA;
-    if (launch_pdl(kernel, dim3(1), dim3(kRouteThreads), smem, stream, logits, m, n_experts, top_k, ids, probs,
-                   expert_offsets, sorted_pairs) != cudaSuccess)
+  // a decode batch: one CTA; a larger batch: the top-k over many CTAs (one warp
+  // per token), then the grouping by one CTA
+  const bool split = m > 32;
+  auto launch = [&](auto kernel, auto topk_kernel) -> nvfp4_status {
+    if (!split) {
+      if (set_smem(kernel, smem) != cudaSuccess) return NVFP4_ERR_CUDA;
+      if (launch_pdl(kernel, dim3(1), dim3(kRouteThreads), smem, stream, logits, m, n_experts, top_k, ids, probs,
+                     expert_offsets, sorted_pairs) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+      return launched();
+    }
+    if (launch_pdl(topk_kernel, dim3(ceil_div(m, kTopkWarps)), dim3(kTopkWarps * 32), 0, stream, logits, m,
+                   n_experts, top_k, ids, probs) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    if (set_smem(moe_group_kernel, smem) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (launch_pdl(moe_group_kernel, dim3(1), dim3(kRouteThreads), smem, stream, static_cast<const int*>(ids),
+                   m * top_k, n_experts, expert_offsets, sorted_pairs) != cudaSuccess)
       return NVFP4_ERR_CUDA;
     return launched();
   };
-  if (nper <= 1) return launch(moe_route_kernel<1>);
-  if (nper <= 2) return launch(moe_route_kernel<2>);
-  if (nper <= 4) return launch(moe_route_kernel<4>);
-  if (nper <= 8) return launch(moe_route_kernel<8>);
-  if (nper <= 16) return launch(moe_route_kernel<16>);
-  return launch(moe_route_kernel<32>);
+  if (nper <= 1) return launch(moe_route_kernel<1>, moe_topk_kernel<1>);
+  if (nper <= 2) return launch(moe_route_kernel<2>, moe_topk_kernel<2>);
+  if (nper <= 4) return launch(moe_route_kernel<4>, moe_topk_kernel<4>);
+  if (nper <= 8) return launch(moe_route_kernel<8>, moe_topk_kernel<8>);
+  if (nper <= 16) return launch(moe_route_kernel<16>, moe_topk_kernel<16>);
+  return launch(moe_route_kernel<32>, moe_topk_kernel<32>);
 }
 
 size_t moe_ffn_workspace_bytes(int32_t m, int32_t top_k, int32_t n_experts, int32_t d, int32_t inter) {
