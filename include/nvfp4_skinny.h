@@ -250,6 +250,22 @@ nvfp4_status lm_head_argmax(const nvfp4_weight *w, const uint16_t *x, int32_t m,
 nvfp4_status lm_head_argmax_noalloc(const nvfp4_weight *w, const uint16_t *x, int32_t m, float *max_logit,
                                     int32_t *argmax, cudaStream_t stream);
 
+/*
+ * The launch plan a product would use, for host-side checks of the work
+ * decomposition (no device work; no CUDA call).
+ *   product  0 dense GEMM (n x k), 1 lm_head (n x k), 2 MoE gate+up (n = 2*inter,
+ *            k = d), 3 MoE down (n = d, k = inter).
+ *   m, top_k, n_experts  as the product's call (top_k, n_experts: MoE only).
+ *   sms      the grid's SM count to plan for (the library plans for the device's).
+ *   out      (host) int32 [10]: K split S, chunks per slice L, ring stages per
+ *            warp, staged chunks per row, staged rows, segments one CTA may
+ *            stage (decode kernel), grid, segment-list capacity, 1 if the
+ *            prefill kernel runs it, dynamic shared memory bytes.
+ * Returns NVFP4_ERR_SHAPE for shapes the product rejects or no plan fits.
+ */
+nvfp4_status nvfp4_plan_info(int32_t product, int32_t m, int32_t n, int32_t k, int32_t top_k, int32_t n_experts,
+                             int32_t sms, int32_t *out, int32_t out_len);
+
 #ifdef __cplusplus
 }
 #endif

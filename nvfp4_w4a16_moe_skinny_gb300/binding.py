@@ -25,7 +25,7 @@ EXPORTS = (
     "nvfp4_status_string", "nvfp4_layout_version", "nvfp4_device_error", "nvfp4_repacked_bytes",
     "nvfp4_quantize_workspace_bytes", "nvfp4_quantize", "nvfp4_repack", "nvfp4_gemm_workspace_bytes",
     "nvfp4_gemm", "moe_route_topk", "moe_ffn_workspace_bytes", "moe_ffn_grouped",
-    "lm_head_workspace_bytes", "lm_head_argmax", "lm_head_argmax_noalloc",
+    "lm_head_workspace_bytes", "lm_head_argmax", "lm_head_argmax_noalloc", "nvfp4_plan_info",
 )
 
 
@@ -89,6 +89,8 @@ def _sig(lib):
     lib.lm_head_workspace_bytes.argtypes = [_I, _I]
     lib.lm_head_argmax.argtypes = [ctypes.POINTER(CWeight), _P, _I, _P, _P, _P, _SZ, _P]
     lib.lm_head_argmax_noalloc.argtypes = [ctypes.POINTER(CWeight), _P, _I, _P, _P, _P]
+    lib.nvfp4_plan_info.argtypes = [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int32), _I]
+    lib.nvfp4_plan_info.restype = ctypes.c_int
     for name in ("nvfp4_quantize", "nvfp4_repack", "nvfp4_gemm", "moe_route_topk", "moe_ffn_grouped",
                  "lm_head_argmax", "lm_head_argmax_noalloc", "nvfp4_device_error"):
         getattr(lib, name).restype = ctypes.c_int

@@ -794,3 +794,39 @@ extern "C" nvfp4_status lm_head_argmax_noalloc(const nvfp4_weight* w, const uint
   if (cudaMemsetAsync(ws, 0, sizeof(unsigned), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
   return lm_head_launch(w, x, m, max_logit, argmax, ws, stream);
 }
+
+// ------------------------------------------------------------------ plan query
+extern "C" nvfp4_status nvfp4_plan_info(int32_t product, int32_t m, int32_t n, int32_t k, int32_t top_k,
+                                        int32_t n_experts, int32_t sms, int32_t* out, int32_t out_len) {
+  if (!out) return NVFP4_ERR_NULL;
+  if (out_len < 10 || sms < 1 || m < 1 || n < 1 || k < 16 || (k % 16)) return NVFP4_ERR_SHAPE;
+  const int ng = ceil_div(n, kGroupRows), kc = ceil_div(k, kTileK);
+  Plan pl;
+  bool ok = false;
+  switch (product) {
+    case 0:  // dense GEMM
+      if (m > 16) return NVFP4_ERR_SHAPE;
+      ok = make_plan(m, dense_split(m, n, k), ng, kc, 1, 0, false, false, sms, &pl);
+      break;
+    case 1:  // lm_head
+      if (m > 16) return NVFP4_ERR_SHAPE;
+      ok = make_plan(m, 1, ng, kc, 1, 0, false, false, sms, &pl);
+      break;
+    case 2:    // MoE gate+up: n = 2 * inter, k = d
+    case 3: {  // MoE down: n = d, k = inter
+      if (top_k < 1 || n_experts < top_k || m > 4096 || m * top_k > 16384) return NVFP4_ERR_SHAPE;
+      const int d = product == 2 ? k : n, inter = product == 2 ? n / 2 : k;
+      const MoESplits sp = moe_splits(m, top_k, n_experts, d, inter, true);
+      ok = make_plan(m, product == 2 ? sp.s_gu : sp.s_dn, ng, kc, sp.n_seg_max, n_experts, sp.per_run, product == 3,
+                     sms, &pl);
+      break;
+    }
+    default:
+      return NVFP4_ERR_SHAPE;
+  }
+  if (!ok) return NVFP4_ERR_SHAPE;
+  const int32_t v[10] = {pl.S,    pl.L,        pl.ns,           pl.xs_chunks, pl.xs_rows, pl.max_cta_segs,
+                         pl.grid, pl.max_segs, pl.per_run ? 1 : 0, static_cast<int32_t>(pl.smem)};
+  for (int i = 0; i < 10; ++i) out[i] = v[i];
+  return NVFP4_OK;
+}
