@@ -53,6 +53,22 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def max_over_ranks(values, dist, device):
+    """Each rank's timings -> their maximum over all ranks (the slowest replica sets
+    the job's time).  dist is torch.distributed or None (one process)."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_gbs(bytes_per_step, ms_per_step, world):
+    """Whole-job weight-GB/s: every replica streams bytes_per_step per step."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 def dense_bytes(n, k):
     return n * k // 2 + n * k // 16
 
@@ -338,13 +354,10 @@ def run_ours(args, rank, world, dist):
         raise RuntimeError("device error flag set during the timed region")
 
     bytes_step = sum(wl["bytes"].values())
-    if dist is not None:
-        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = t.tolist()
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dist, dev)
     ms_step = total_ms / args.steps
-    value = world * bytes_step / (ms_step * 1e-3) / 1e9
-    e2e_value = world * bytes_step / (e2e_ms / args.steps * 1e-3) / 1e9
+    value = job_gbs(bytes_step, ms_step, world)
+    e2e_value = job_gbs(bytes_step, e2e_ms / args.steps, world)
     peak, peak_kind = peaks()
     lm_bytes = wl["bytes"]["lm_head"]
     achieved = lm_bytes / (lm_us * 1e-6) / 1e9
