@@ -448,7 +448,9 @@ def time_prefill(lib, wl, args, dev, stream):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"m": m, "ms_per_layer": round(ms, 4), "tokens_per_s": round(m / (ms * 1e-3), 1),
             "weight_bytes": nbytes, "active_experts": active, "max_pairs_per_expert": int(counts.max()),
-            "weight_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4), "launches_per_layer": 4}
+            "weight_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
+            # router (top-k grid + grouping grid above 32 tokens), gate+up, down, combine
+            "launches_per_layer": 5 if m > 32 else 4}
 
 
 def load_traffic(kernel, m):
