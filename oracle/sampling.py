@@ -13,8 +13,9 @@ easy as 1, 2, 3", SC 2011), written here from its definition: ten rounds of two
 XORed with the round key and the other words, the key bumped by the Weyl
 constants between rounds.  The draw for vocabulary row n of token m under a
 64-bit seed is word 0 of Philox(counter = (n, m, 0, 0), key = (seed low, seed
-high)); u = ((word >> 8) + 0.5) / 2^24 -- the top 24 bits, so that u is exact in
-fp32 as well and lies strictly inside (0, 1) -- and g = -log(-log u).
+high)); u = ((word >> 9) + 0.5) / 2^23 -- the top 23 bits, so that u (a 24-bit
+odd multiple of 2^-24) is exact in fp32 as well and lies strictly inside (0, 1)
+-- and g = -log(-log u).
 """
 
 from __future__ import annotations
@@ -53,9 +54,9 @@ def philox4x32_10(counter, key):
 
 
 def uniform_open(word):
-    """uint32 -> a float in (0, 1): ((word >> 8) + 0.5) / 2^24 (exact in fp32 and fp64)."""
-    w = np.asarray(word, np.uint64) >> np.uint64(8)
-    return (w.astype(np.float64) + 0.5) * 2.0 ** -24
+    """uint32 -> a float in (0, 1): ((word >> 9) + 0.5) / 2^23 (exact in fp32 and fp64)."""
+    w = np.asarray(word, np.uint64) >> np.uint64(9)
+    return (w.astype(np.float64) + 0.5) * 2.0 ** -23
 
 
 def gumbel(word):

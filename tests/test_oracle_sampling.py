@@ -24,15 +24,18 @@ def test_philox_known_answer_vectors():
 
 
 def test_gumbel_is_the_inverse_cdf():
-    words = np.array([0, 1, 2 ** 31, 2 ** 32 - 1, 123456789], np.uint64)
+    words = np.array([0, 1, 2 ** 31, 2 ** 32 - 1, 123456789], np.uint64)   # g stays finite at both ends
     u = OS.uniform_open(words)
     assert np.all(u > 0) and np.all(u < 1)
     g = OS.gumbel(words)
     assert np.allclose(np.exp(-np.exp(-g)), u, rtol=1e-12)          # the Gumbel CDF at g is u
-    assert OS.uniform_open(np.array([0], np.uint64))[0] == 0.5 * 2.0 ** -24          # smallest u
-    assert OS.uniform_open(np.array([2 ** 32 - 1], np.uint64))[0] == 1 - 0.5 * 2.0 ** -24  # largest u
-    half = OS.gumbel(np.array([2 ** 31], np.uint64))[0]               # u = (2^23 + 0.5) / 2^24
-    assert half == pytest.approx(-np.log(-np.log(0.5 + 2.0 ** -25)), abs=1e-12)
+    assert OS.uniform_open(np.array([0], np.uint64))[0] == 0.5 * 2.0 ** -23          # smallest u
+    assert OS.uniform_open(np.array([2 ** 32 - 1], np.uint64))[0] == 1 - 0.5 * 2.0 ** -23  # largest u
+    # every u is exactly representable in fp32 (24 significant bits)
+    us = OS.uniform_open(np.array([0, 1 << 9, 2 ** 31, 2 ** 32 - 1, 0xDEADBEEF], np.uint64))
+    assert np.array_equal(us.astype(np.float32).astype(np.float64), us)
+    half = OS.gumbel(np.array([2 ** 31], np.uint64))[0]               # u = (2^22 + 0.5) / 2^23
+    assert half == pytest.approx(-np.log(-np.log(0.5 + 2.0 ** -24)), abs=1e-12)
     assert half == pytest.approx(-np.log(np.log(2.0)), abs=1e-6)
 
 
