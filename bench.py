@@ -329,6 +329,7 @@ def run_ours(args, rank, world, dist):
     kernel_us = {name: 1e3 * statistics.mean(a.elapsed_time(b) for a, b in ev[name]) for name, _ in calls}
 
     prefill = time_prefill(lib, wl, args, dev, stream) if args.prefill_m > 0 else None
+    sampling = time_sampling(lib, wl, bufs, m, args, dev, stream)
 
     # ---- end to end through the public API with host buffers (copies inside the timed region)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -396,6 +397,7 @@ def run_ours(args, rank, world, dist):
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "graph_ms_per_step": round(graph_ms, 4) if graph_ms else None,
         "prefill": prefill,
+        "lm_head_sample": sampling,
         "gpu_launches": launches_per_step * args.steps,
         "timing": "value: steps back to back, events around the region; kernels_us: a second pass with events "
                   "around every call",
@@ -404,6 +406,34 @@ def run_ours(args, rank, world, dist):
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         result["cpu_baseline"] = cpu_baseline(m, seconds=args.cpu_seconds)
     return result
+
+
+def time_sampling(lib, wl, bufs, m, args, dev, stream):
+    """The lm_head with fused Gumbel-max temperature sampling (T = 1) at the step's M,
+    back to back with events on the launching stream, each launch a new seed."""
+    import torch
+    key = torch.empty((m,), dtype=torch.float32, device=dev)
+    tok = torch.empty((m,), dtype=torch.int32, device=dev)
+    fns = [lib.plan_lm_head_sample(wl["lm_head"], bufs["x_lm"], 1.0, 1000 + s, key, tok, stream)
+           for s in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for fn in fns[:args.warmup]:
+            fn()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for fn in fns:
+            fn()
+        e1.record(stream)
+    stream.synchronize()
+    if lib.device_error() != 0:
+        raise RuntimeError("device error flag set during the sampling timing")
+    us = 1e3 * e0.elapsed_time(e1) / len(fns)
+    nbytes = step_bytes(wl, 0)["lm_head"]
+    peak, _ = peaks()
+    return {"m": m, "temperature": 1.0, "us_per_launch": round(us, 2),
+            "weight_gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / peak, 4)}
 
 
 def time_prefill(lib, wl, args, dev, stream):

@@ -225,6 +225,24 @@ nvfp4_status lm_head_argmax(const nvfp4_weight *w, const uint16_t *x, int32_t m,
                             int32_t *argmax, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * lm_head with fused temperature sampling (Gumbel-max): for each token row m, the
+ * n maximising (W_hat . x_m)[n] / temperature + g(n, m), with g standard Gumbel
+ * noise, and that maximum -- a draw from softmax(logits / temperature); ties to
+ * the lower n.  gemma-cuda-hybrid README, "Server": Gumbel-max temperature
+ * sampling, temperature 0 reducing to exact greedy.  The noise is the
+ * counter-based generator Philox4x32-10 (Salmon et al., SC 2011): word 0 of
+ * Philox(counter (n, m, 0, 0), key (seed low 32 bits, seed high 32 bits)), u =
+ * ((word >> 9) + 0.5) / 2^23, g = -log(-log u).  A call is deterministic in its
+ * seed: pass a new seed for each step.  No logits or noise reach memory.
+ *   temperature  > 0 samples; == 0 is lm_head_argmax (max_key = the max logit).
+ *   max_key      (device) fp32 [m]: the winning logit / temperature + noise.
+ *   token        (device) int32 [m].
+ *   everything else as lm_head_argmax (same workspace).
+ */
+nvfp4_status lm_head_sample(const nvfp4_weight *w, const uint16_t *x, int32_t m, float temperature, uint64_t seed,
+                            float *max_key, int32_t *token, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * lm_head_argmax without a caller-provided workspace.  The pages have no
  * counterpart to this call: it exists for callers that cannot allocate device
  * memory -- for example a plugin or runtime that hands the library only its

@@ -26,6 +26,7 @@ EXPORTS = (
     "nvfp4_quantize_workspace_bytes", "nvfp4_quantize", "nvfp4_repack", "nvfp4_gemm_workspace_bytes",
     "nvfp4_gemm", "moe_route_topk", "moe_ffn_workspace_bytes", "moe_ffn_grouped",
     "lm_head_workspace_bytes", "lm_head_argmax", "lm_head_argmax_noalloc", "nvfp4_plan_info",
+    "lm_head_sample",
 )
 
 
@@ -89,6 +90,9 @@ def _sig(lib):
     lib.lm_head_workspace_bytes.argtypes = [_I, _I]
     lib.lm_head_argmax.argtypes = [ctypes.POINTER(CWeight), _P, _I, _P, _P, _P, _SZ, _P]
     lib.lm_head_argmax_noalloc.argtypes = [ctypes.POINTER(CWeight), _P, _I, _P, _P, _P]
+    lib.lm_head_sample.argtypes = [ctypes.POINTER(CWeight), _P, _I, ctypes.c_float, ctypes.c_uint64, _P, _P, _P, _SZ,
+                                   _P]
+    lib.lm_head_sample.restype = ctypes.c_int
     lib.nvfp4_plan_info.argtypes = [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int32), _I]
     lib.nvfp4_plan_info.restype = ctypes.c_int
     for name in ("nvfp4_quantize", "nvfp4_repack", "nvfp4_gemm", "moe_route_topk", "moe_ffn_grouped",
@@ -199,6 +203,36 @@ class Library:
             ctypes.byref(cw), x.data_ptr(), m, out[0].data_ptr(), out[1].data_ptr(), ws.data_ptr(), ws.numel(),
             _stream(stream)))
         return out
+
+    def lm_head_sample(self, w: Weight, x: torch.Tensor, temperature: float, seed: int, out=None, stream=None):
+        """Gumbel-max sample per token row: returns (max key, token)."""
+        m = x.shape[0]
+        if out is None:
+            out = (torch.empty((m,), dtype=torch.float32, device=x.device),
+                   torch.empty((m,), dtype=torch.int32, device=x.device))
+        ws = self.workspace("lm_head", self.lib.lm_head_workspace_bytes(m, w.n), x.device)
+        cw = w.c()
+        self._check("lm_head_sample", self.lib.lm_head_sample(
+            ctypes.byref(cw), x.data_ptr(), m, float(temperature), int(seed) & (2 ** 64 - 1), out[0].data_ptr(),
+            out[1].data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
+        return out
+
+    def plan_lm_head_sample(self, w: Weight, x: torch.Tensor, temperature: float, seed: int, max_key, token,
+                            stream=None):
+        """lm_head_sample as a zero-argument callable (arguments marshalled once)."""
+        m = x.shape[0]
+        ws = self.workspace("lm_head", self.lib.lm_head_workspace_bytes(m, w.n), x.device)
+        cw = w.c()
+        args = (ctypes.byref(cw), x.data_ptr(), m, float(temperature), int(seed) & (2 ** 64 - 1), max_key.data_ptr(),
+                token.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream))
+        fn = self.lib.lm_head_sample
+
+        def run():
+            st = fn(*args)
+            if st:
+                raise NVFP4Error("lm_head_sample", st)
+        run.keep = (cw, ws)
+        return run
 
     def route_topk(self, logits: torch.Tensor, top_k: int, out=None, stream=None):
         m, e = logits.shape

@@ -28,6 +28,33 @@ constexpr unsigned kErrWaitTimeout = 1u;
 // ~1 s at 2 GHz: far above any legitimate wait for a bulk copy.
 constexpr long long kWaitCycles = 2000000000ll;
 
+// Word 0 of the counter-based generator Philox4x32-10 (Salmon, Moraes, Dror,
+// Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011) for the counter
+// (c0, c1, 0, 0) and key (k0, k1): ten rounds, each two 32x32 -> 64-bit products
+// by the generator's multipliers, the high halves crossed and XORed with the
+// other words and the round key, the key bumped by the Weyl increments between
+// rounds.
+__device__ __forceinline__ uint32_t philox4x32_10_word0(uint32_t c0, uint32_t c1, uint32_t k0, uint32_t k1) {
+  uint32_t c2 = 0, c3 = 0;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) k0 += 0x9E3779B9u, k1 += 0xBB67AE85u;
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0, c1 = lo1, c2 = n2, c3 = lo0;
+  }
+  return c0;
+}
+
+// Standard Gumbel noise -log(-log u) from a 32-bit draw, u = ((w >> 9) + 0.5) / 2^23:
+// (w >> 9) + 0.5 needs 24 significant bits, so u is exact in fp32 and lies
+// strictly inside (0, 1).
+__device__ __forceinline__ float gumbel_from_bits(uint32_t w) {
+  const float u = (static_cast<float>(w >> 9) + 0.5f) * (1.0f / 8388608.0f);
+  return -logf(-logf(u));
+}
+
 // Bytes of dynamic shared memory this launch was given.
 __device__ __forceinline__ uint32_t dynamic_smem_bytes() {
   uint32_t r;

@@ -50,7 +50,8 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kMaxCtaSegs = 8;                 // segments whose units one CTA may hold
 constexpr int kMaxStagedRows = kMaxCtaSegs * 16;
 
-enum { kEpiStore = 0, kEpiArgmax = 1, kEpiGated = 2, kEpiRows = 3 };
+// kEpiSample: the argmax of logit / T + Gumbel noise (temperature sampling)
+enum { kEpiStore = 0, kEpiArgmax = 1, kEpiGated = 2, kEpiRows = 3, kEpiSample = 4 };
 constexpr int kSharedSeg = -1;  // segment of the always-on shared expert
 constexpr int kDenseSeg = -2;   // the single segment of a dense job
 
@@ -88,6 +89,8 @@ struct Job {
   int xs_rows;            // staged-activation capacity: rows (plus the zero row)
   int max_cta_segs;       // segments one CTA may touch (<= kMaxCtaSegs)
   int max_segs;           // prefill kernel: capacity of the segment list
+  float inv_temp;         // kEpiSample: 1 / temperature
+  uint32_t seed_lo, seed_hi;  // kEpiSample: the Philox key of this call's noise
 };
 
 __host__ __device__ inline size_t stream_table_bytes(int n_experts) {
@@ -363,9 +366,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if constexpr (kEpi == kEpiRows) {
           const int out = slot_out[sl * 16 + slot];
           if ((kMMA || t4 == 0) && out >= 0 && row < p.n) p.yf[static_cast<size_t>(out) * p.yf_ld + row] = v;
-        } else if constexpr (kEpi == kEpiArgmax) {
+        } else if constexpr (kEpi == kEpiArgmax || kEpi == kEpiSample) {
           const int b = kMMA ? c * 2 + (i & 1) : c;
-          if (row < p.n && better(v, row, bv[b], bi[b])) bv[b] = v, bi[b] = row;
+          float key = v;  // the logit, or (sampling) logit / T + the Gumbel noise of (row, token)
+          if constexpr (kEpi == kEpiSample)
+            if (row < p.n && slot < p.m)
+              key = fmaf(v, p.inv_temp, gumbel_from_bits(philox4x32_10_word0(row, slot, p.seed_lo, p.seed_hi)));
+          if (row < p.n && better(key, row, bv[b], bi[b])) bv[b] = key, bi[b] = row;
         } else {  // kEpiGated: rows g = gate i, g+8 = up i of block rb, i = rb*8 + g
           if (hrow == 0) {
             const float up = a[c][kMMA ? i + 2 : 1];
@@ -497,11 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc[a][c][i] = v * mul[sl * 16 + (kMMA ? c * 8 + 2 * t4 + (i & 1) : c)];
           }
       }
-      if (kEpi == kEpiArgmax || p.S == 1) {  // the lm_head never splits K
+      if (kEpi == kEpiArgmax || kEpi == kEpiSample || p.S == 1) {  // the lm_head never splits K
 #pragma unroll
         for (int a = 0; a < 4; ++a)
           if (a < pc.tn) finish_tile(sl, pc.grp, pc.t0 + a, acc[a]);
-      } else if constexpr (kEpi != kEpiArgmax) {
+      } else if constexpr (kEpi != kEpiArgmax && kEpi != kEpiSample) {
         // ---- k-split: per tile, store the partial and take a ticket; the last of
         // the S slices sums all S partials in slice order and finishes the tile
         const size_t cell0 = (static_cast<size_t>(pc.seg) * p.ng + pc.grp) * 4 + pc.t0;
@@ -585,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if constexpr (kEpi == kEpiArgmax) {
+  if constexpr (kEpi == kEpiArgmax || kEpi == kEpiSample) {
     // ---- lanes -> warp (ties to the lower row)
 #pragma unroll
     for (int b = 0; b < NBEST; ++b) {

@@ -512,8 +512,9 @@ namespace nvfp4 {
 namespace {
 
 // The lm_head never splits K: a split would put partial logits in memory.
+// The lm_head grid: greedy argmax, or (temperature > 0) the Gumbel-max sample.
 nvfp4_status lm_head_launch(const nvfp4_weight* w, const uint16_t* x, int32_t m, float* max_logit, int32_t* argmax,
-                            void* ws, cudaStream_t stream) {
+                            void* ws, cudaStream_t stream, float temperature = 0.f, uint64_t seed = 0) {
   Job p = dense_job(w, x, m);
   p.am_cnt = static_cast<unsigned*>(ws);
   p.am_val = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes);
@@ -524,6 +525,11 @@ nvfp4_status lm_head_launch(const nvfp4_weight* w, const uint16_t* x, int32_t m,
   if (!make_plan(m, 1, p.ng, p.kc, 1, 0, false, false, std::max(1, sm_count()), &plan)) return NVFP4_ERR_SHAPE;
   WeightMaps maps;
   if (!make_maps(w, nullptr, &maps)) return NVFP4_ERR_CUDA;
+  if (temperature > 0.f) {
+    p.inv_temp = 1.f / temperature;
+    p.seed_lo = static_cast<uint32_t>(seed), p.seed_hi = static_cast<uint32_t>(seed >> 32);
+    return dispatch_stream<kEpiSample>(p, maps, plan, stream);
+  }
   return dispatch_stream<kEpiArgmax>(p, maps, plan, stream);
 }
 
@@ -542,6 +548,18 @@ nvfp4_status lm_head_argmax(const nvfp4_weight* w, const uint16_t* x, int32_t m,
   if (!aligned(ws, 16)) return NVFP4_ERR_ALIGN;
   if (sm_count() > 1024) return NVFP4_ERR_SHAPE;
   return lm_head_launch(w, x, m, max_logit, argmax, ws, stream);
+}
+
+nvfp4_status lm_head_sample(const nvfp4_weight* w, const uint16_t* x, int32_t m, float temperature, uint64_t seed,
+                            float* max_key, int32_t* token, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (const nvfp4_status st = check_weight(w, 1, 0)) return st;
+  if (!x || !max_key || !token) return NVFP4_ERR_NULL;
+  if (m < 1 || m > 16 || !(temperature >= 0.f) || !(temperature < INFINITY)) return NVFP4_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(max_key, 4) || !aligned(token, 4)) return NVFP4_ERR_ALIGN;
+  if (!ws || ws_bytes < lm_head_workspace_bytes(m, w->n)) return NVFP4_ERR_WORKSPACE;
+  if (!aligned(ws, 16)) return NVFP4_ERR_ALIGN;
+  if (sm_count() > 1024) return NVFP4_ERR_SHAPE;
+  return lm_head_launch(w, x, m, max_key, token, ws, stream, temperature, seed);
 }
 
 }  // extern "C"
