@@ -106,6 +106,13 @@ def test_lm_head_and_moe_argument_errors(so):
     assert so.lm_head_argmax(ctypes.byref(w), p, 1, None, p, p, 1 << 20, None) == 1
     assert so.lm_head_argmax(ctypes.byref(w), p, 17, p, p, p, 1 << 20, None) == 2
     assert so.lm_head_argmax(ctypes.byref(w), p, 1, p, p, p, 8, None) == 4
+    # the sampling lm_head: the same checks, and the temperature must be finite and >= 0
+    assert so.lm_head_sample(ctypes.byref(w), p, 1, 1.0, 7, None, p, p, 1 << 20, None) == 1
+    assert so.lm_head_sample(ctypes.byref(w), p, 17, 1.0, 7, p, p, p, 1 << 20, None) == 2
+    assert so.lm_head_sample(ctypes.byref(w), p, 1, -0.5, 7, p, p, p, 1 << 20, None) == 2
+    assert so.lm_head_sample(ctypes.byref(w), p, 1, float("nan"), 7, p, p, p, 1 << 20, None) == 2
+    assert so.lm_head_sample(ctypes.byref(w), p, 1, float("inf"), 7, p, p, p, 1 << 20, None) == 2
+    assert so.lm_head_sample(ctypes.byref(w), p, 1, 1.0, 7, p, p, p, 8, None) == 4
     assert so.moe_route_topk(p, 15, 128, 0, p, p, p, p, None) == 2           # top_k < 1
     assert so.moe_route_topk(p, 15, 4, 8, p, p, p, p, None) == 2             # top_k > n_experts
     assert so.moe_route_topk(p, 15, 2048, 8, p, p, p, p, None) == 2          # n_experts > 1024
