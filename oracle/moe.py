@@ -32,16 +32,27 @@ import numpy as np
 from .formats import dequantize_matrix, bf16_round
 
 
-def route_topk(logits: np.ndarray, top_k: int):
-    """Per token: ids of the top_k largest logits (ties -> lower id) and softmax over them.
+def route_topk(logits: np.ndarray, top_k: int, softmax_all: bool = False, expert_scale=None):
+    """Per token: ids of the top_k largest logits (ties -> lower id) and their weights.
 
+    Default: the softmax over the top_k chosen logits.  softmax_all: the literal
+    topK(softmax(logits)) of TensorSharp docs/models/gemma4.md, "3.2 Per-layer
+    (MoE)" -- the softmax over all experts' logits, read at the chosen experts
+    (not renormalised).  expert_scale [E]: each weight times its expert's scale
+    (a per-expert down-projection scale folded into the routing weights, same
+    page, "14. Optimization opportunities").
     Returns (ids int32 [M, top_k] in descending-logit order, probs float64 [M, top_k]).
     """
     l = np.asarray(logits, dtype=np.float64)
     order = np.argsort(-l, axis=1, kind="stable")[:, :top_k]
     chosen = np.take_along_axis(l, order, axis=1)
     z = np.exp(chosen - chosen[:, :1])
-    probs = z / np.sum(z, axis=1, keepdims=True)
+    if softmax_all:
+        probs = z / np.sum(np.exp(l - chosen[:, :1]), axis=1, keepdims=True)
+    else:
+        probs = z / np.sum(z, axis=1, keepdims=True)
+    if expert_scale is not None:
+        probs = probs * np.asarray(expert_scale, np.float64)[order]
     return order.astype(np.int32), probs
 
 
@@ -81,7 +92,8 @@ def expert_ffn(wgu_hat: np.ndarray, wd_hat: np.ndarray, x: np.ndarray):
     return hb, d_out, d_abs
 
 
-def moe_layer(x, logits, top_k, gate_up, down, shared_gate_up=None, shared_down=None):
+def moe_layer(x, logits, top_k, gate_up, down, shared_gate_up=None, shared_down=None, softmax_all=False,
+              expert_scale=None):
     """The whole MoE FFN layer.
 
     gate_up = (nib [E, 2I, d/2], scales [E, 2I, d/16], g [E]); down likewise for [E, d, I];
@@ -92,7 +104,7 @@ def moe_layer(x, logits, top_k, gate_up, down, shared_gate_up=None, shared_down=
     x = np.asarray(x, np.float64)
     m, d = x.shape
     n_exp = gate_up[0].shape[0]
-    ids, probs = route_topk(logits, top_k)
+    ids, probs = route_topk(logits, top_k, softmax_all, expert_scale)
     counts, offsets, sorted_pairs = group_by_expert(ids, n_exp)
     out = np.zeros((m, d))
     tol = np.zeros((m, d))

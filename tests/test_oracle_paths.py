@@ -73,6 +73,24 @@ def test_route_topk_brute_force_and_ties():
     assert np.all(np.diff(probs, axis=1) <= 0)
 
 
+def test_route_weight_options_closed_forms():
+    """softmax_all: with logits ln 1 .. ln 4 the softmax over all four experts is
+    1/10 .. 4/10, so the top-2 weights are 0.4 and 0.3 (not renormalised); the
+    default renormalises the chosen two to 4/7 and 3/7; an expert scale multiplies
+    the weight of its expert only; with top_k = E both readings coincide."""
+    logits = np.log(np.array([[1.0, 2.0, 3.0, 4.0]]))
+    ids, p_all = MO.route_topk(logits, 2, softmax_all=True)
+    assert ids.tolist() == [[3, 2]]
+    assert np.allclose(p_all, [[0.4, 0.3]], rtol=1e-14)
+    _, p_renorm = MO.route_topk(logits, 2)
+    assert np.allclose(p_renorm, [[4 / 7, 3 / 7]], rtol=1e-14)
+    _, p_scaled = MO.route_topk(logits, 2, softmax_all=True, expert_scale=[1.0, 1.0, 0.5, 2.0])
+    assert np.allclose(p_scaled, [[0.8, 0.15]], rtol=1e-14)
+    rng = np.random.default_rng(9)
+    l = rng.standard_normal((5, 6))
+    assert np.allclose(MO.route_topk(l, 6, softmax_all=True)[1], MO.route_topk(l, 6)[1], rtol=1e-12)
+
+
 def test_grouping_brute_force():
     rng = np.random.default_rng(3)
     ids = np.stack([rng.choice(16, 4, replace=False) for _ in range(9)]).astype(np.int32)
