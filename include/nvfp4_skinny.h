@@ -183,6 +183,24 @@ nvfp4_status moe_route_topk(const float *logits, int32_t m, int32_t n_experts, i
                             cudaStream_t stream);
 
 /*
+ * moe_route_topk with the routing-weight variants of TensorSharp
+ * docs/models/gemma4.md: the same top_k ids and grouping, and
+ *   flags & NVFP4_ROUTE_SOFTMAX_ALL: probs = the softmax over all n_experts
+ *       logits read at the chosen experts (the literal topK(softmax(logits)) of
+ *       "3.2 Per-layer (MoE)"; not renormalised, so a row sums to at most 1);
+ *       otherwise the softmax over the top_k chosen logits.
+ *   expert_scale (device) fp32 [n_experts] or NULL: each pair's weight times its
+ *       expert's scale (a per-expert down-projection scale folded into the
+ *       routing weights, "14. Optimization opportunities").
+ * moe_ffn_grouped then applies these weights unchanged.  Other flag bits:
+ * NVFP4_ERR_SHAPE.
+ */
+#define NVFP4_ROUTE_SOFTMAX_ALL 1
+nvfp4_status moe_route_topk_ex(const float *logits, int32_t m, int32_t n_experts, int32_t top_k, int32_t flags,
+                               const float *expert_scale, int32_t *ids, float *probs, int32_t *expert_offsets,
+                               int32_t *sorted_pairs, cudaStream_t stream);
+
+/*
  * Grouped MoE FFN: out[t] = bf16( sum_r probs[t,r] * down_e(h_{t,r}) + shared_down(h_{t,shared}) )
  * with h = bf16( gelu_tanh(gate_e . x_t) * (up_e . x_t) ) and e = ids[t, r].
  *   x               (device) bf16 [m, d], 16-byte aligned.

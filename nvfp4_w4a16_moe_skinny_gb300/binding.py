@@ -26,7 +26,7 @@ EXPORTS = (
     "nvfp4_quantize_workspace_bytes", "nvfp4_quantize", "nvfp4_repack", "nvfp4_gemm_workspace_bytes",
     "nvfp4_gemm", "moe_route_topk", "moe_ffn_workspace_bytes", "moe_ffn_grouped",
     "lm_head_workspace_bytes", "lm_head_argmax", "lm_head_argmax_noalloc", "nvfp4_plan_info",
-    "lm_head_sample",
+    "lm_head_sample", "moe_route_topk_ex",
 )
 
 
@@ -82,6 +82,8 @@ def _sig(lib):
     lib.nvfp4_gemm_workspace_bytes.argtypes = [_I, _I, _I]
     lib.nvfp4_gemm.argtypes = [ctypes.POINTER(CWeight), _P, _I, _P, _P, _SZ, _P]
     lib.moe_route_topk.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P]
+    lib.moe_route_topk_ex.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]
+    lib.moe_route_topk_ex.restype = ctypes.c_int
     lib.moe_ffn_workspace_bytes.restype = _SZ
     lib.moe_ffn_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
     lib.moe_ffn_grouped.argtypes = [_P, _I, _I, _P, _P, _P, ctypes.POINTER(CWeight), ctypes.POINTER(CWeight),
@@ -234,7 +236,8 @@ class Library:
         run.keep = (cw, ws)
         return run
 
-    def route_topk(self, logits: torch.Tensor, top_k: int, out=None, stream=None):
+    def route_topk(self, logits: torch.Tensor, top_k: int, out=None, stream=None, softmax_all: bool = False,
+                   expert_scale: torch.Tensor = None):
         m, e = logits.shape
         if out is None:
             dev = logits.device
@@ -243,9 +246,15 @@ class Library:
                    torch.empty((e + 1,), dtype=torch.int32, device=dev),
                    torch.empty((m * top_k,), dtype=torch.int32, device=dev))
         ids, probs, offsets, pairs = out
-        self._check("moe_route_topk", self.lib.moe_route_topk(
-            logits.data_ptr(), m, e, top_k, ids.data_ptr(), probs.data_ptr(), offsets.data_ptr(), pairs.data_ptr(),
-            _stream(stream)))
+        if not softmax_all and expert_scale is None:
+            self._check("moe_route_topk", self.lib.moe_route_topk(
+                logits.data_ptr(), m, e, top_k, ids.data_ptr(), probs.data_ptr(), offsets.data_ptr(),
+                pairs.data_ptr(), _stream(stream)))
+        else:
+            self._check("moe_route_topk_ex", self.lib.moe_route_topk_ex(
+                logits.data_ptr(), m, e, top_k, 1 if softmax_all else 0,
+                expert_scale.data_ptr() if expert_scale is not None else None, ids.data_ptr(), probs.data_ptr(),
+                offsets.data_ptr(), pairs.data_ptr(), _stream(stream)))
         return out
 
     def moe_ffn(self, x, top_k, probs, offsets, pairs, gate_up: Weight, down: Weight, shared_gate_up: Weight = None,

@@ -28,11 +28,18 @@ namespace nvfp4 {
 // phase 2 in one.  NPER: logits per lane (n_experts <= 32 * NPER).
 constexpr int kRouteThreads = 1024;
 
+// Routing weight options (moe_route_topk_ex): the softmax over all experts read
+// at the chosen ones (not renormalised over the top_k).
+constexpr int kRouteSoftmaxAll = 1;
+
 // Top-k + softmax of token t by one warp; lane r < top_k writes the r-th choice
-// (and, when s_ids is given, also into shared memory).
+// (and, when s_ids is given, also into shared memory).  With kRouteSoftmaxAll the
+// denominator sums every expert's exp; escale (nullable) scales each weight by
+// its expert's entry.
 template <int NPER>
 __device__ __forceinline__ void token_topk(const float* __restrict__ logits, int t, int n_experts, int top_k, int lane,
-                                           int* __restrict__ ids, float* __restrict__ probs, int* s_ids) {
+                                           int* __restrict__ ids, float* __restrict__ probs, int* s_ids, int flags,
+                                           const float* __restrict__ escale) {
   {
     const float* row = logits + static_cast<size_t>(t) * n_experts;
     float lv[NPER];  // experts lane + 32*i, read once
@@ -61,15 +68,23 @@ __device__ __forceinline__ void token_topk(const float* __restrict__ logits, int
       if (lane == (be & 31)) taken |= 1u << (be >> 5);
       if (lane == r) myv = bv, mye = be;
     }
-    // softmax over the chosen logits (round 0 holds the maximum)
+    // softmax over the chosen logits, or over all of them (round 0 holds the maximum)
     const float vmax = __shfl_sync(0xffffffffu, myv, 0);
     const float ez = lane < top_k ? expf(myv - vmax) : 0.f;
     float z = ez;
+    if (flags & kRouteSoftmaxAll) {
+      z = 0.f;
+#pragma unroll
+      for (int i = 0; i < NPER; ++i)
+        if (lane + 32 * i < n_experts) z += expf(lv[i] - vmax);
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
     if (lane < top_k) {
+      float pr = ez / z;
+      if (escale) pr *= __ldg(escale + mye);
       ids[t * top_k + lane] = mye;
-      probs[t * top_k + lane] = ez / z;
+      probs[t * top_k + lane] = pr;
       if (s_ids) s_ids[t * top_k + lane] = mye;
     }
   }
@@ -203,8 +218,9 @@ __device__ __forceinline__ void group_pairs_hist(const int* s_ids, int pairs, in
 // A decode batch: one CTA does both (one warp per token, then the grouping).
 template <int NPER>
 __global__ void __launch_bounds__(kRouteThreads, 1)
-    moe_route_kernel(const float* __restrict__ logits, int m, int n_experts, int top_k, int* __restrict__ ids,
-                     float* __restrict__ probs, int* __restrict__ offsets, int* __restrict__ sorted_pairs) {
+    moe_route_kernel(const float* __restrict__ logits, int m, int n_experts, int top_k, int flags,
+                     const float* __restrict__ escale, int* __restrict__ ids, float* __restrict__ probs,
+                     int* __restrict__ offsets, int* __restrict__ sorted_pairs) {
   extern __shared__ int route_smem[];
   const int pairs = m * top_k;
   int* s_ids = route_smem;                                  // [pairs]
@@ -214,7 +230,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   const int nwarps = blockDim.x >> 5;
   pdl_wait();  // the logits may come from the previous grid
   pdl_launch_dependents();
-  for (int t = warp; t < m; t += nwarps) token_topk<NPER>(logits, t, n_experts, top_k, lane, ids, probs, s_ids);
+  for (int t = warp; t < m; t += nwarps)
+    token_topk<NPER>(logits, t, n_experts, top_k, lane, ids, probs, s_ids, flags, escale);
   __syncthreads();
   // (at most 32 tokens: the ballot sort; the histogram passes cost more here)
   group_pairs(s_ids, pairs, n_experts, s_cnt, s_wsum, offsets, sorted_pairs);
@@ -225,12 +242,12 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 constexpr int kTopkWarps = 8;
 template <int NPER>
 __global__ void __launch_bounds__(kTopkWarps * 32)
-    moe_topk_kernel(const float* __restrict__ logits, int m, int n_experts, int top_k, int* __restrict__ ids,
-                    float* __restrict__ probs) {
+    moe_topk_kernel(const float* __restrict__ logits, int m, int n_experts, int top_k, int flags,
+                    const float* __restrict__ escale, int* __restrict__ ids, float* __restrict__ probs) {
   const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
   pdl_wait();  // the logits may come from the previous grid
   pdl_launch_dependents();
-  if (t < m) token_topk<NPER>(logits, t, n_experts, top_k, threadIdx.x & 31, ids, probs, nullptr);
+  if (t < m) token_topk<NPER>(logits, t, n_experts, top_k, threadIdx.x & 31, ids, probs, nullptr, flags, escale);
 }
 
 // A prefill chunk, step 2: the grouping of all pairs by one CTA (the histogram

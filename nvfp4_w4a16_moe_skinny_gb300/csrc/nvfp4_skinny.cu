@@ -642,6 +642,14 @@ extern "C" {
 
 nvfp4_status moe_route_topk(const float* logits, int32_t m, int32_t n_experts, int32_t top_k, int32_t* ids,
                             float* probs, int32_t* expert_offsets, int32_t* sorted_pairs, cudaStream_t stream) {
+  return moe_route_topk_ex(logits, m, n_experts, top_k, 0, nullptr, ids, probs, expert_offsets, sorted_pairs, stream);
+}
+
+nvfp4_status moe_route_topk_ex(const float* logits, int32_t m, int32_t n_experts, int32_t top_k, int32_t flags,
+                               const float* expert_scale, int32_t* ids, float* probs, int32_t* expert_offsets,
+                               int32_t* sorted_pairs, cudaStream_t stream) {
+  if (flags & ~kRouteSoftmaxAll) return NVFP4_ERR_SHAPE;
+  if (expert_scale && !aligned(expert_scale, 4)) return NVFP4_ERR_ALIGN;
   if (!logits || !ids || !probs || !expert_offsets || !sorted_pairs) return NVFP4_ERR_NULL;
   if (m < 1 || m > 4096 || top_k < 1 || top_k > 32 || n_experts < top_k || n_experts > 1024 ||
       m * top_k > 16384)
@@ -657,13 +665,13 @@ nvfp4_status moe_route_topk(const float* logits, int32_t m, int32_t n_experts, i
   auto launch = [&](auto kernel, auto topk_kernel) -> nvfp4_status {
     if (!split) {
       if (set_smem(kernel, smem) != cudaSuccess) return NVFP4_ERR_CUDA;
-      if (launch_pdl(kernel, dim3(1), dim3(kRouteThreads), smem, stream, logits, m, n_experts, top_k, ids, probs,
-                     expert_offsets, sorted_pairs) != cudaSuccess)
+      if (launch_pdl(kernel, dim3(1), dim3(kRouteThreads), smem, stream, logits, m, n_experts, top_k,
+                     static_cast<int>(flags), expert_scale, ids, probs, expert_offsets, sorted_pairs) != cudaSuccess)
         return NVFP4_ERR_CUDA;
       return launched();
     }
     if (launch_pdl(topk_kernel, dim3(ceil_div(m, kTopkWarps)), dim3(kTopkWarps * 32), 0, stream, logits, m,
-                   n_experts, top_k, ids, probs) != cudaSuccess)
+                   n_experts, top_k, static_cast<int>(flags), expert_scale, ids, probs) != cudaSuccess)
       return NVFP4_ERR_CUDA;
     if (set_smem(moe_group_kernel, smem) != cudaSuccess) return NVFP4_ERR_CUDA;
     if (launch_pdl(moe_group_kernel, dim3(1), dim3(kRouteThreads), smem, stream, static_cast<const int*>(ids),

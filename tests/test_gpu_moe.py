@@ -33,6 +33,37 @@ def test_route_topk_bit_exact(lib, m, e, k):
     assert np.max(np.abs(probs - oprobs)) <= PROB_TOL
 
 
+@pytest.mark.parametrize("m,e,k,softmax_all,scaled", [(1, 128, 8, True, False), (15, 128, 8, True, True),
+                                                       (15, 128, 8, False, True), (100, 40, 3, True, True),
+                                                       (512, 128, 8, True, True)])
+def test_route_weight_options(lib, m, e, k, softmax_all, scaled):
+    """The softmax over all experts (not renormalised) and a per-expert scale folded
+    into the weights: ids and grouping unchanged and bit-exact, weights as the oracle's
+    (one CTA for m <= 32, the split router above)."""
+    logits = W.normal_f32((m, e), W.seed_of("route-opt", m, e, k))
+    scale = (0.5 + np.abs(W.normal_f32((e,), W.seed_of("route-scale", e)))).astype(np.float32) if scaled else None
+    ids, probs, offsets, pairs = lib.route_topk(upload_f32(logits), k, softmax_all=softmax_all,
+                                                expert_scale=upload_f32(scale) if scaled else None)
+    torch.cuda.synchronize()
+    oids, oprobs = OM.route_topk(logits, k, softmax_all, scale)
+    _, ooffsets, opairs = OM.group_by_expert(oids, e)
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    assert np.array_equal(offsets.cpu().numpy(), ooffsets)
+    assert np.array_equal(pairs.cpu().numpy(), opairs)
+    # fp32 exp and a sum over up to 128 terms against float64: a few 1e-6 relative
+    assert np.max(np.abs(probs.cpu().numpy() - oprobs) / np.maximum(oprobs, 1e-30)) <= 2e-5
+
+
+def test_moe_layer_with_weight_options(lib):
+    """The whole layer on routing weights from the variants: softmax over all experts
+    and per-expert scales, for a decode batch and a prefill chunk."""
+    scale = (0.5 + np.abs(W.normal_f32((8,), 77))).astype(np.float32)
+    for m in (5, 40):
+        got, ref, _ = _moe_case(lib, m, 128, 64, 8, 3, True, "moe-small", softmax_all=True, expert_scale=scale)
+        check_bound(got, ref["out"], ref["tol_scale"], True, f"moe weight options m={m}")
+    assert lib.device_error() == 0
+
+
 def test_route_ties_go_to_lower_id(lib):
     logits = np.zeros((4, 128), np.float32)
     logits[0, [3, 77, 9, 100]] = 2.0          # four-way tie at the top
@@ -74,7 +105,8 @@ def _experts(lib, case, shared):
     return _EXPERTS[key]
 
 
-def _moe_case(lib, m, d, inter, n_exp, top_k, shared, tag, logits=None, rows=None):
+def _moe_case(lib, m, d, inter, n_exp, top_k, shared, tag, logits=None, rows=None, softmax_all=False,
+              expert_scale=None):
     """Run the layer on the GPU for all m tokens; the oracle computes the tokens in
     `rows` (all by default) -- a token's output depends on its own x and logits only."""
     case = W.MoECase(m=m, d=d, inter=inter, n_experts=n_exp, top_k=top_k, tag=tag)
@@ -83,7 +115,9 @@ def _moe_case(lib, m, d, inter, n_exp, top_k, shared, tag, logits=None, rows=Non
     if logits is None:
         logits = case.logits()
     x = upload_bf16(xb)
-    ids, probs, offsets, pairs = lib.route_topk(upload_f32(logits), top_k)
+    scale_dev = upload_f32(expert_scale) if expert_scale is not None else None
+    ids, probs, offsets, pairs = lib.route_topk(upload_f32(logits), top_k, softmax_all=softmax_all,
+                                                expert_scale=scale_dev)
     out = lib.moe_ffn(x, top_k, probs, offsets, pairs, wgu, wdn, sgu, sdn)
     torch.cuda.synchronize()
     got = bf16_to_f64(out)
@@ -92,7 +126,7 @@ def _moe_case(lib, m, d, inter, n_exp, top_k, shared, tag, logits=None, rows=Non
         xf, logits, got = xf[rows], logits[rows], got[rows]
     # oracle: quantize only the experts the (sampled) routing uses, plus the shared one
     oids, _ = OM.route_topk(logits, top_k)
-    used = sorted(set(oids.reshape(-1).tolist()))
+    used = sorted(set(oids.reshape(-1).tolist()))  # (the options change the weights, not the ids)
     gq = [None] * n_exp
     dq = [None] * n_exp
     for e in used:
@@ -106,7 +140,7 @@ def _moe_case(lib, m, d, inter, n_exp, top_k, shared, tag, logits=None, rows=Non
     down = (np.stack([q[0] for q in dq]), np.stack([q[1] for q in dq]), np.array([q[2] for q in dq]))
     sh_gu = F.quantize_matrix(case.gate_up(-1)) if shared else None
     sh_dn = F.quantize_matrix(case.down(-1)) if shared else None
-    ref = OM.moe_layer(xf.astype(np.float64), logits, top_k, gate_up, down, sh_gu, sh_dn)
+    ref = OM.moe_layer(xf.astype(np.float64), logits, top_k, gate_up, down, sh_gu, sh_dn, softmax_all, expert_scale)
     return got, ref, (ids, offsets, pairs)
 
 
