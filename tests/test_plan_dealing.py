@@ -213,3 +213,30 @@ def test_plan_query_rejects_bad_shapes(so):
     assert so.nvfp4_plan_info(4, 1, 64, 64, 0, 0, 152, out, 10) == 2    # unknown product
     assert so.nvfp4_plan_info(2, 1, 128, 64, 9, 8, 152, out, 10) == 2   # top_k > n_experts
     assert so.nvfp4_plan_info(0, 1, 64, 64, 0, 0, 152, None, 10) == 1
+
+
+def test_random_shapes_always_get_a_valid_plan(so):
+    """Shapes the ABI accepts, drawn at random (seeded): the planner returns a plan for
+    each, and the plan passes the decomposition checks under a random routing."""
+    rng = random.Random(2026)
+    for _ in range(40):
+        m = rng.randint(1, 16)
+        n = rng.randint(1, 300) * rng.choice([1, 16, 64])
+        k = 16 * rng.randint(1, 400)
+        sms = rng.choice([152, 148, 132, 16])
+        check_decode(plan_of(so, 0, m, n, k, sms=sms), m, cdiv(n, 64), cdiv(k, 64), [m], False)
+    for _ in range(25):
+        m = rng.choice([1, 2, 7, 15, 16, 17, 31, 33, 64, 200, 512])
+        n_exp = rng.choice([2, 8, 40, 128, 256])
+        top_k = rng.randint(1, min(8, n_exp))
+        d, inter = 64 * rng.randint(1, 48), 64 * rng.randint(1, 16)
+        sms = rng.choice([152, 16])
+        counts = routings(m, top_k, n_exp, seed=rng.randint(0, 10 ** 6))[0]
+        blk = 32 if m > 16 else 16
+        blocks = [min(blk, c - blk * b) for c in counts for b in range(cdiv(c, blk))]
+        for product, nn, kk in ((2, 2 * inter, d), (3, d, inter)):
+            plan = plan_of(so, product, m, nn, kk, top_k, n_exp, sms)
+            if m > 16:
+                check_prefill(plan, cdiv(nn, 64), cdiv(kk, 64), blocks + [min(blk, m - blk * b) for b in range(cdiv(m, blk))])
+            else:
+                check_decode(plan, m, cdiv(nn, 64), cdiv(kk, 64), [c for c in counts if c > 0] + [m], product == 3)
