@@ -34,9 +34,10 @@
  *     failure returns NVFP4_ERR_CUDA (the CUDA error is left for
  *     cudaGetLastError()).  No C++ exception crosses this boundary.
  *   - bf16 tensors are passed as uint16_t bit patterns, row-major, contiguous.
- *   - Preconditions not checked on the device: inputs are finite; expert ids
- *     passed to moe_ffn_grouped come from moe_route_topk; workspaces are not
- *     shared by calls that may run concurrently.
+ *   - Preconditions not checked on the device: weights and activations are
+ *     finite; router logits are finite or -inf (a NaN logit counts as -inf);
+ *     expert ids passed to moe_ffn_grouped come from moe_route_topk;
+ *     workspaces are not shared by calls that may run concurrently.
  *   - Kernel waits are bounded (about one second); a wait that runs out sets a
  *     bit in a device error word read by nvfp4_device_error().
  */
@@ -119,11 +120,15 @@ nvfp4_status nvfp4_device_error(uint32_t *out, int32_t clear);
 size_t nvfp4_repacked_bytes(int32_t n, int32_t k, int32_t num_matrices);
 
 /*
- * Offline quantizer (formula (1) in reverse), deciding in IEEE fp32:
- *   g = amax|W| / 2688; per 16-group t = (bmax / 6) / g, scale = E4M3
- *   round-to-nearest-even saturating at 448; element = E2M1
- *   round-to-nearest-even saturating at 6 of w / (e4m3(scale) * g); a group
- *   whose scale is 0 gets zero codes; an all-zero matrix gets g = 0.
+ * Offline quantizer (formula (1) in reverse):
+ *   g = fp32(amax|W| / 2688) (one correctly rounded fp32 division); per
+ *   16-group the scale is the E4M3 code nearest to the exact quotient
+ *   bmax / (6 g), ties to even, saturating at 448; each element the E2M1 code
+ *   nearest to the exact quotient w / (e4m3(scale) * g), ties to even,
+ *   saturating at 6, with the sign of w kept; a group whose scale is 0 gets
+ *   zero codes; an all-zero matrix gets g = 0.  (The quotients are float64
+ *   divisions by exact divisors, which decide every code as the exact real
+ *   quotient would.)
  *   w        (device) fp32 [num_matrices, n, k], k % 16 == 0.
  *   nibbles  (device) u8 [num_matrices, n, k/2], canonical: column 2i in the
  *            low nibble of byte i.
@@ -177,6 +182,9 @@ nvfp4_status nvfp4_gemm(const nvfp4_weight *w, const uint16_t *x, int32_t m, uin
  *                   ascending within an expert.
  * Limits: 1 <= m <= 4096, 1 <= top_k <= 32, top_k <= n_experts <= 1024,
  * m * top_k <= 16384.
+ * Logits: finite or -inf; a NaN counts as -inf.  Every id is a valid expert
+ * (the top_k picks are distinct: -inf logits go to the lowest unchosen ids),
+ * and a token whose logits are all -inf gets weight 0 on every slot.
  */
 nvfp4_status moe_route_topk(const float *logits, int32_t m, int32_t n_experts, int32_t top_k, int32_t *ids,
                             float *probs, int32_t *expert_offsets, int32_t *sorted_pairs,
@@ -237,6 +245,8 @@ nvfp4_status moe_ffn_grouped(const uint16_t *x, int32_t m, int32_t top_k, const 
  *   x          (device) bf16 [m, w->k], 1 <= m <= 16, 16-byte aligned.
  *   max_logit  (device) fp32 [m];  argmax (device) int32 [m].
  *   ws         (device) lm_head_workspace_bytes(m, n) bytes, 8-byte aligned.
+ * A NaN logit counts as -inf, so the index is always a valid row: a token whose
+ * logits are all NaN gets (-inf, 0).
  */
 size_t lm_head_workspace_bytes(int32_t m, int32_t vocab);
 nvfp4_status lm_head_argmax(const nvfp4_weight *w, const uint16_t *x, int32_t m, float *max_logit,

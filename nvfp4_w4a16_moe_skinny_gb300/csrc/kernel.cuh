@@ -372,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (kEpi == kEpiSample)
             if (row < p.n && slot < p.m)
               key = fmaf(v, p.inv_temp, gumbel_from_bits(philox4x32_10_word0(row, slot, p.seed_lo, p.seed_hi)));
+          if (key != key) key = -INFINITY;  // a NaN counts as -inf: the result is always a valid row
           if (row < p.n && better(key, row, bv[b], bi[b])) bv[b] = key, bi[b] = row;
         } else {  // kEpiGated: rows g = gate i, g+8 = up i of block rb, i = rb*8 + g
           if (hrow == 0) {

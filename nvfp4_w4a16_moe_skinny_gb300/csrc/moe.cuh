@@ -42,12 +42,16 @@ __device__ __forceinline__ void token_topk(const float* __restrict__ logits, int
                                            const float* __restrict__ escale) {
   {
     const float* row = logits + static_cast<size_t>(t) * n_experts;
-    float lv[NPER];  // experts lane + 32*i, read once
+    float lv[NPER];  // experts lane + 32*i, read once; a NaN logit counts as -inf
 #pragma unroll
     for (int i = 0; i < NPER; ++i) {
       const int e = lane + 32 * i;
-      lv[i] = e < n_experts ? __ldg(row + e) : -INFINITY;
+      const float v = e < n_experts ? __ldg(row + e) : -INFINITY;
+      lv[i] = v == v ? v : -INFINITY;
     }
+    // Every valid logit is >= -inf, so each round's winner is a valid expert not
+    // chosen before (top_k <= n_experts): when all that remain are -inf, the lowest
+    // such id.
     uint32_t taken = 0;  // bit i: expert lane + 32*i already chosen
     float myv = -INFINITY;
     int mye = 0;
@@ -68,20 +72,22 @@ __device__ __forceinline__ void token_topk(const float* __restrict__ logits, int
       if (lane == (be & 31)) taken |= 1u << (be >> 5);
       if (lane == r) myv = bv, mye = be;
     }
-    // softmax over the chosen logits, or over all of them (round 0 holds the maximum)
+    // softmax over the chosen logits, or over all of them (round 0 holds the maximum);
+    // a token whose logits are all -inf (or NaN) gets weight 0 on every slot
     const float vmax = __shfl_sync(0xffffffffu, myv, 0);
-    const float ez = lane < top_k ? expf(myv - vmax) : 0.f;
+    const bool none = vmax == -INFINITY;
+    const float ez = lane < top_k && !none ? expf(myv - vmax) : 0.f;
     float z = ez;
     if (flags & kRouteSoftmaxAll) {
       z = 0.f;
 #pragma unroll
       for (int i = 0; i < NPER; ++i)
-        if (lane + 32 * i < n_experts) z += expf(lv[i] - vmax);
+        if (lane + 32 * i < n_experts && !none) z += expf(lv[i] - vmax);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
     if (lane < top_k) {
-      float pr = ez / z;
+      float pr = none ? 0.f : ez / z;
       if (escale) pr *= __ldg(escale + mye);
       ids[t * top_k + lane] = mye;
       probs[t * top_k + lane] = pr;

@@ -2,9 +2,14 @@
 //
 // Quantizer: formula (1) of nvfp4_skinny.h in reverse (E2M1 weights, E4M3
 // group-16 scales, fp32 global scale -- gemma-cuda-hybrid README, "Everything
-// it has / Inference engine").  Every quotient is an IEEE fp32 operation and
-// the code decisions use the hardware round-to-nearest-even saturating
-// converters, so the codes are a function of fp32 values only.
+// it has / Inference engine").  The codes are the round-to-nearest-even codes
+// of the exact quotients bmax / (6 g) and w / (e4m3(s) g): each quotient is one
+// float64 division by an exact divisor, narrowed to fp32 with round-to-odd and
+// handed to the hardware round-to-nearest-even saturating converter.  The
+// grids' midpoints have at most 5 significant bits and a quotient of fp32
+// values that is not a midpoint lies at least 2^-32 (relative) from every
+// midpoint, so one float64 rounding cannot move it across one; round-to-odd to
+// 24 bits followed by rounding to at most 5 bits is the correctly rounded result.
 //
 // Repack: canonical bytes -> the tiled layout documented in nvfp4_skinny.h
 // ("offline weight repack into mma-fragment order" -- gemma-cuda-hybrid README,
@@ -60,6 +65,14 @@ __device__ __forceinline__ uint32_t e2m1x2_code_rne(float lo, float hi) {
   return r;
 }
 
+// double -> float, round to odd: truncate, and set the lowest significand bit
+// when the truncation was inexact.  A later round-to-nearest-even to 22 or fewer
+// significant bits then equals rounding the double directly.
+__device__ __forceinline__ float f64_to_f32_round_odd(double x) {
+  const float f = __double2float_rz(x);
+  return static_cast<double>(f) == x ? f : __uint_as_float(__float_as_uint(f) | 1u);
+}
+
 __device__ __forceinline__ float e4m3_value(uint32_t c) {
   const uint32_t e = (c >> 3) & 0xF, m = c & 7;
   const float mag = e == 0 ? static_cast<float>(m) * 0.001953125f  // m/8 * 2^-6
@@ -91,18 +104,19 @@ __global__ void quant_groups_kernel(const float* __restrict__ w, int n, int k, c
 #pragma unroll
     for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
     uint32_t s_code = 0;
-    float denom = 0.f;
+    double denom = 0.0;
     if (g > 0.f) {
-      const float t = __fdiv_rn(__fdiv_rn(bmax, 6.0f), g);
-      s_code = e4m3_code_rne(t);
-      denom = __fmul_rn(e4m3_value(s_code), g);
+      const double t = static_cast<double>(bmax) / (6.0 * static_cast<double>(g));  // exact divisor
+      s_code = e4m3_code_rne(f64_to_f32_round_odd(t));
+      denom = static_cast<double>(e4m3_value(s_code)) * static_cast<double>(g);      // exact product
     }
     uint32_t packed[2] = {0u, 0u};
-    if (denom > 0.f) {
+    if (denom > 0.0) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint32_t b = e2m1x2_code_rne(__fdiv_rn(v[2 * i], denom), __fdiv_rn(v[2 * i + 1], denom));
-        packed[i >> 2] |= b << (8 * (i & 3));
+        const float lo = f64_to_f32_round_odd(static_cast<double>(v[2 * i]) / denom);
+        const float hi = f64_to_f32_round_odd(static_cast<double>(v[2 * i + 1]) / denom);
+        packed[i >> 2] |= e2m1x2_code_rne(lo, hi) << (8 * (i & 3));
       }
     }
     uint2* dst = reinterpret_cast<uint2*>(nibbles + (static_cast<size_t>(e) * n * k) / 2 + gi * 8);

@@ -7,19 +7,23 @@ dequant, ... the group-16 scale handling"):
 
     w_hat[n, k] = e2m1(q[n, k]) * e4m3(s[n, k // 16]) * g
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 
 * E2M1 code c = sign<<3 | exp<<1 | man, bias 1, one subnormal (0.5), no
   inf/NaN, so the magnitudes are {0, 0.5, 1, 1.5, 2, 3, 4, 6}.
 * E4M3 is the "fn" variant: bias 7, subnormals m/8 * 2^-6, max 448, codes
   0x7F/0xFF are NaN, no infinities.
-* Global scale g = fp32(amax / (448 * 6)) is the dequant multiplier.
-* Block scale code = E4M3 round-to-nearest-even, saturating at 448, of
-  t = (bmax / 6) / g; element code = E2M1 round-to-nearest-even, saturating at
-  6, of v = w / (e4m3(scale) * g).  Every one of these quotients is taken in
-  IEEE fp32 (the precision the library's quantize kernel decides in), so the
-  integer codes are a function of fp32 values; the rounding to the code grid
-  is then exact.
+* Global scale g = fp32(amax / (448 * 6)) is the dequant multiplier: an FP32
+  number, the correctly rounded quotient.
+* Block scale code = E4M3 round-to-nearest-even, saturating at 448, of the
+  exact quotient t = bmax / (6 g); element code = E2M1 round-to-nearest-even,
+  saturating at 6, of the exact quotient v = w / (e4m3(scale) * g).  Both are
+  computed as one float64 division whose divisor (6 g, or e4m3(scale) * g, at
+  most 28 significant bits) is exact.  The grids' midpoints have at most 5
+  significant bits, and a quotient of fp32 values that is not a midpoint lies
+  at least 2^-32 (relative) away from every midpoint, far beyond the 2^-53 of
+  one float64 rounding: so the rounded quotient takes the same code decision
+  as the exact real one.
 * A block whose scale decodes to 0 gets all-zero codes (no division).
 * An all-zero matrix gets g = 0 and all-zero codes and scales.
 * Canonical packing: element 2i in the low nibble, 2i+1 in the high nibble of
@@ -64,8 +68,8 @@ def e4m3_value(code) -> np.ndarray:
 def e4m3_encode_nonneg(t) -> np.ndarray:
     """Round non-negative finite values to the E4M3 grid, ties to even, saturate at 448.
 
-    Exact: every fp32 input and every grid midpoint is exact in float64, so the
-    comparisons implied by ``np.rint`` (round half to even) decide exactly.
+    Exact for the float64 value given: scaling by a power of two is exact and
+    ``np.rint`` rounds half to even, so the code is the RNE code of that value.
     """
     t = np.minimum(np.asarray(t, dtype=np.float64), E4M3_MAX)
     code = np.zeros(t.shape, dtype=np.int64)
@@ -86,25 +90,25 @@ def e4m3_encode_nonneg(t) -> np.ndarray:
 
 
 def e2m1_encode(v) -> np.ndarray:
-    """Round finite values to the E2M1 grid, ties to even, saturate at +-6; keeps the sign bit."""
+    """Round finite values to the E2M1 grid, ties to even, saturate at +-6; keeps the sign bit.
+
+    The magnitude code is the number of grid midpoints below |v|: midpoint i lies
+    between magnitude codes i and i + 1 and counts when |v| exceeds it, or equals
+    it and code i + 1 is even (round half to even).  Past the last midpoint the
+    code is 7 (6.0), which is the saturation.
+    """
     v = np.asarray(v, dtype=np.float64)
-    neg = np.signbit(v)
-    a = np.minimum(np.abs(v), E2M1_MAX)
-    code = np.zeros(a.shape, dtype=np.int64)
-    small = a < 1.0
-    code[small] = np.rint(a[small] * 2.0).astype(np.int64)   # 0, 1 (=0.5) or 2 (=1.0)
-    big = ~small
-    if np.any(big):
-        ab = a[big]
-        _, ex = np.frexp(ab)
-        e = ex.astype(np.int64) - 1          # 0, 1 or 2
-        q = np.rint(np.ldexp(ab, 1 - e))     # mantissa in units of 2^(e-1): [2, 4]
-        carry = q >= 4
-        e = np.where(carry, e + 1, e)
-        q = np.where(carry, 2, q)
-        code[big] = ((e + 1) << 1) | (q.astype(np.int64) - 2)
-    code = code | (neg.astype(np.int64) << 3)
-    return code.astype(np.uint8)
+    a = np.abs(v)
+    mags = e2m1_value(np.arange(8))
+    code = np.zeros(a.shape, dtype=np.uint8)
+    for i in range(7):
+        mid = (mags[i] + mags[i + 1]) / 2
+        if (i + 1) % 2 == 0:
+            code += a >= mid
+        else:
+            code += a > mid
+    code |= np.signbit(v).astype(np.uint8) << 3
+    return code
 
 
 # --------------------------------------------------------------------------- quantizer
@@ -139,14 +143,15 @@ def quantize_matrix(w: np.ndarray, chunk_rows: int = 4096):
 
 def _quantize_rows(w: np.ndarray, g: np.float32):
     n, k = w.shape
-    blocks = w.reshape(n, k // 16, 16)
-    bmax = np.max(np.abs(blocks), axis=2).astype(np.float32)
-    t = (bmax / np.float32(E2M1_MAX)).astype(np.float32) / g          # two fp32 divisions
-    s_code = e4m3_encode_nonneg(t.astype(np.float32))
-    s_val = e4m3_value(s_code).astype(np.float32)                      # exact in fp32
-    denom = (s_val * g).astype(np.float32)                             # one fp32 product
-    safe = np.where(denom == 0, np.float32(1), denom)
-    v = (blocks / safe[:, :, None]).astype(np.float32)                 # fp32 division
+    g64 = np.float64(g)
+    blocks = w.astype(np.float64).reshape(n, k // 16, 16)
+    bmax = np.max(np.abs(blocks), axis=2)
+    t = bmax / (E2M1_MAX * g64)                     # exact divisor; decision = the exact quotient's
+    s_code = e4m3_encode_nonneg(t)
+    s_val = e4m3_value(s_code)
+    denom = s_val * g64                             # exact (at most 28 significant bits)
+    safe = np.where(denom == 0, 1.0, denom)
+    v = blocks / safe[:, :, None]
     q = e2m1_encode(v)
     q = np.where((s_val == 0)[:, :, None], np.uint8(0), q).reshape(n, k)
     nib = (q[:, 0::2] & 0xF) | ((q[:, 1::2] & 0xF) << 4)

@@ -3,8 +3,8 @@
 The pages say only that weights are repacked once, offline, "into
 mma-fragment order" so kernel loads are 16-byte coalesced
 (gemma-cuda-hybrid README, "Everything it has / Inference engine" and
-"NVFP4-specific").  The layout itself is this library's; its specification
-(restated in DESIGN.md, "Data layout in HBM") is, for layout version 2:
+"NVFP4-specific").  The layout itself is this library's; its specification,
+for layout version 2, is:
 
 * Rows are padded to a multiple of 64, K to a multiple of 64, with zero bytes.
 * A *gated* matrix [gate || up] with N = 2I (I % 32 == 0) first has its rows

@@ -14,7 +14,7 @@ Sources (page title, section):
 * TensorFold issue #1048, "Steps", step 2: the activation is GELU-tanh.
 * gemma-cuda-hybrid README, "What it is": 128 experts, top-8 + 1 shared.
 
-Readings (listed in the design doc): top-8 is taken on the raw logits (descending,
+Readings where the pages leave a step open: top-8 is taken on the raw logits (descending,
 ties to the lower expert id) and the softmax runs over the 8 chosen logits;
 this picks the same set as softmax-then-top-k and equals renormalising the
 chosen softmax weights.  The shared expert has the same shape as a routed
@@ -41,16 +41,23 @@ def route_topk(logits: np.ndarray, top_k: int, softmax_all: bool = False, expert
     (not renormalised).  expert_scale [E]: each weight times its expert's scale
     (a per-expert down-projection scale folded into the routing weights, same
     page, "14. Optimization opportunities").
+    A NaN logit counts as -inf; -inf logits are chosen last, lowest id first, and a
+    token whose logits are all -inf gets weight 0 on every slot.
     Returns (ids int32 [M, top_k] in descending-logit order, probs float64 [M, top_k]).
     """
     l = np.asarray(logits, dtype=np.float64)
+    l = np.where(np.isnan(l), -np.inf, l)          # a NaN logit counts as -inf
     order = np.argsort(-l, axis=1, kind="stable")[:, :top_k]
     chosen = np.take_along_axis(l, order, axis=1)
-    z = np.exp(chosen - chosen[:, :1])
+    top = chosen[:, :1]
+    none = np.isneginf(top)                        # every logit -inf: weight 0 everywhere
+    shift = np.where(none, 0.0, top)
+    z = np.where(none, 0.0, np.exp(chosen - shift))
     if softmax_all:
-        probs = z / np.sum(np.exp(l - chosen[:, :1]), axis=1, keepdims=True)
+        den = np.sum(np.exp(l - shift), axis=1, keepdims=True)
     else:
-        probs = z / np.sum(z, axis=1, keepdims=True)
+        den = np.sum(z, axis=1, keepdims=True)
+    probs = np.where(none, 0.0, z / np.where(none, 1.0, den))
     if expert_scale is not None:
         probs = probs * np.asarray(expert_scale, np.float64)[order]
     return order.astype(np.int32), probs

@@ -45,3 +45,31 @@ def check_bound(got: np.ndarray, exact: np.ndarray, abs_scale: np.ndarray, bf16_
 
 def ragged_weight(n, k, seed):
     return W.weight((n, k), seed)
+
+
+def oracle_quantize(w: np.ndarray):
+    """The oracle's canonical NVFP4 bytes of one fp32 matrix [N, K] or a stack [E, N, K]:
+    (nibbles, scales, global scales float32 [E] or scalar)."""
+    from oracle import formats as F
+    if w.ndim == 2:
+        return F.quantize_matrix(w)
+    return F.quantize_stack(w)
+
+
+def upload_oracle_weight(lib, q, gated: bool = False):
+    """Repack the oracle's canonical bytes on the GPU into the kernel layout: the kernels
+    then read exactly the codes the oracle computes with."""
+    nib, sc, g = q
+    g = np.atleast_1d(np.asarray(g, np.float32))
+    return lib.repack(torch.from_numpy(np.ascontiguousarray(nib)).to(dev()),
+                      torch.from_numpy(np.ascontiguousarray(sc)).to(dev()),
+                      torch.from_numpy(g).to(dev()), gated=gated)
+
+
+def assert_gpu_quantizer_matches(lib, w: np.ndarray, q, what: str):
+    """The library's GPU quantizer gives the oracle's bytes for this matrix (stack)."""
+    nib, sc, g = lib.quantize(upload_f32(w))
+    onib, osc, og = q
+    assert np.array_equal(np.atleast_1d(g.cpu().numpy()), np.atleast_1d(np.asarray(og, np.float32))), what
+    assert np.array_equal(sc.cpu().numpy(), osc), f"{what}: scale codes differ"
+    assert np.array_equal(nib.cpu().numpy(), onib), f"{what}: element codes differ"

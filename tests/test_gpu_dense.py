@@ -12,12 +12,17 @@ from oracle import gemm as OG
 from oracle import layout as OL
 from oracle import lm_head as OLM
 from nvfp4_w4a16_moe_skinny_gb300 import workloads as W
-from tests.gpu_helpers import bf16_to_f64, check_bound, dev, upload_bf16, upload_f32
+from tests.gpu_helpers import (assert_gpu_quantizer_matches, bf16_to_f64, check_bound, dev, oracle_quantize,
+                               upload_bf16, upload_f32, upload_oracle_weight)
+from tests.test_oracle_formats import _near_midpoint_matrix
 
 pytestmark = pytest.mark.gpu
 
 
 # ------------------------------------------------------------------ quantizer
+# The GPU quantizer and the oracle both decide every code as the round-to-nearest-even
+# code of the exact quotient (bmax / (6 g) for a scale, w / (e4m3(s) g) for an
+# element); the oracle is pinned to a brute force over exact rationals.
 
 @pytest.mark.parametrize("n,k,seed", [(512, 256, 0), (40, 80, 1), (33, 16, 2), (16, 1024, 3)])
 def test_quantizer_bit_exact(lib, n, k, seed):
@@ -49,6 +54,18 @@ def test_quantizer_special_values(lib):
     assert np.array_equal(nib.cpu().numpy(), onib)
     z_nib, z_sc, z_g = lib.quantize(torch.zeros((16, 32), device=dev()))
     assert z_g.item() == 0.0 and not z_nib.any().item() and not z_sc.any().item()
+
+
+def test_quantizer_near_midpoints(lib):
+    """Block maxima and elements on, and one fp32 step either side of, the exact rounding
+    midpoints under a global scale with a full 24-bit significand: the GPU codes are the
+    exact quotients' codes (IEEE fp32 quotients would pick other codes for some)."""
+    w = _near_midpoint_matrix()
+    nib, sc, g = lib.quantize(upload_f32(w))
+    onib, osc, og = F.quantize_matrix(w)
+    assert g.item() == float(og)
+    assert np.array_equal(sc.cpu().numpy(), osc)
+    assert np.array_equal(nib.cpu().numpy(), onib)
 
 
 def test_quantizer_stacked(lib):
@@ -92,22 +109,23 @@ def test_repack_folds_negative_scales(lib):
 def _dense(lib, m, n, k, w_seed, x_seed):
     w = W.weight((n, k), w_seed)
     xb, _ = W.activations((m, k), x_seed)
-    wt = lib.prepare(upload_f32(w))
+    nib, sc, g = F.quantize_matrix(w)
+    wt = upload_oracle_weight(lib, (nib, sc, g))
     y = lib.gemm(wt, upload_bf16(xb))
     torch.cuda.synchronize()
-    nib, sc, g = F.quantize_matrix(w)
     exact, _, absy = OG.nvfp4_gemm(nib, sc, g, W.bf16_bits_to_f32(xb).astype(np.float64))
     return bf16_to_f64(y), exact, absy
 
 
 def test_tiny_gemm_config0(lib):
+    """The 512 x 256 matrix quantized by the oracle; the kernel reads the oracle's bytes."""
     case = W.DenseCase.tiny()
     w = case.w()
     xb, xf = case.x()
-    wt = lib.prepare(upload_f32(w))
+    nib, sc, g = F.quantize_matrix(w)
+    wt = upload_oracle_weight(lib, (nib, sc, g))
     y = lib.gemm(wt, upload_bf16(xb))
     torch.cuda.synchronize()
-    nib, sc, g = F.quantize_matrix(w)
     exact, _, absy = OG.nvfp4_gemm(nib, sc, g, xf.astype(np.float64))
     check_bound(bf16_to_f64(y), exact, absy, True, "tiny gemm")
     assert lib.device_error() == 0
@@ -120,16 +138,30 @@ def test_gemm_ragged_all_m(lib, m, n, k):
     check_bound(got, exact, absy, True, f"gemm m={m} n={n} k={k}")
 
 
-@pytest.mark.parametrize("m", [1, 4, 15, 16])
+_DENSE_FULL = {}
+
+
+def _dense_full(lib, n):
+    """The config-1 weight of N rows: the oracle's bytes repacked on the GPU for the
+    kernel, after checking that the GPU quantizer gives the same bytes at full size."""
+    if n not in _DENSE_FULL:
+        _DENSE_FULL.clear()
+        w = W.DenseCase.sweep(1, n).w()
+        q = oracle_quantize(w)
+        assert_gpu_quantizer_matches(lib, w, q, f"config1 n={n}")
+        _DENSE_FULL[n] = (upload_oracle_weight(lib, q), q)
+        torch.cuda.synchronize()
+    return _DENSE_FULL[n]
+
+
 @pytest.mark.parametrize("n", [4096, 14336])
+@pytest.mark.parametrize("m", [1, 4, 15, 16])
 def test_gemm_config1_full_size(lib, m, n):
     case = W.DenseCase.sweep(m, n)
-    w = case.w()
+    wt, (nib, sc, g) = _dense_full(lib, n)
     xb, xf = case.x()
-    wt = lib.prepare(upload_f32(w))
     y = lib.gemm(wt, upload_bf16(xb))
     torch.cuda.synchronize()
-    nib, sc, g = F.quantize_matrix(w)
     exact, _, absy = OG.nvfp4_gemm(nib, sc, g, xf.astype(np.float64))
     check_bound(bf16_to_f64(y), exact, absy, True, f"config1 m={m} n={n}")
     assert lib.device_error() == 0
@@ -200,16 +232,39 @@ def test_lm_head_planted_max_and_tie(lib):
     assert np.array_equal(idx.cpu().numpy(), ref["argmax"])
 
 
+@pytest.mark.parametrize("m", [3, 9])
+def test_lm_head_nan_token_row(lib, m):
+    """A token row of NaN activations makes every logit of that token NaN, which counts
+    as -inf: the result is (-inf, row 0); the other tokens are unaffected (CUDA-core and
+    tensor-core paths)."""
+    vocab, k = 2048, 256
+    w = W.weight((vocab, k), 91)
+    xb, xf = W.activations((m, k), 92)
+    xb = xb.copy()
+    xb[1, :] = 0x7FC0                       # bf16 quiet NaN
+    q = F.quantize_matrix(w)
+    wt = upload_oracle_weight(lib, q)
+    mx, idx = lib.lm_head_argmax(wt, upload_bf16(xb))
+    torch.cuda.synchronize()
+    assert idx[1].item() == 0 and mx[1].item() == float("-inf")
+    keep = [t for t in range(m) if t != 1]
+    ref = OLM.lm_head_argmax(*q, xf[keep].astype(np.float64))
+    _check_argmax(mx.cpu().numpy()[keep], idx.cpu().numpy()[keep], ref, (*q, xf[keep]), "lm_head NaN row")
+    assert lib.device_error() == 0
+
+
 @pytest.fixture(scope="module")
 def lm_head_full(lib):
-    """The full 262,144 x 2,816 lm_head: GPU-quantized for the kernel, oracle-quantized
-    on the host for the reference (the two quantizers are compared bit for bit on
-    sampled rows here and exhaustively on smaller shapes above)."""
+    """The full 262,144 x 2,816 lm_head quantized by the oracle; the kernel reads the
+    oracle's bytes (repacked on the GPU).  The GPU quantizer's bytes for the whole
+    matrix are checked equal to the oracle's on the way."""
     case = W.LMHeadCase(m=1)
     w = case.w_rows(0, case.vocab)
-    wt = lib.prepare(upload_f32(w))
-    nib, sc, g = F.quantize_matrix(w)
+    q = oracle_quantize(w)
+    assert_gpu_quantizer_matches(lib, w, q, "lm_head 262144x2816")
+    wt = upload_oracle_weight(lib, q)
     torch.cuda.synchronize()
+    nib, sc, g = q
     return wt, nib, sc, g
 
 

@@ -7,7 +7,8 @@ import torch
 from oracle import formats as F
 from oracle import moe as OM
 from nvfp4_w4a16_moe_skinny_gb300 import workloads as W
-from tests.gpu_helpers import bf16_to_f64, check_bound, dev, upload_bf16, upload_f32
+from tests.gpu_helpers import (assert_gpu_quantizer_matches, bf16_to_f64, check_bound, dev, upload_bf16,
+                               upload_f32, upload_oracle_weight)
 
 pytestmark = pytest.mark.gpu
 
@@ -64,6 +65,31 @@ def test_moe_layer_with_weight_options(lib):
     assert lib.device_error() == 0
 
 
+@pytest.mark.parametrize("m", [4, 40])
+def test_route_nan_and_neginf_logits(lib, m):
+    """NaN logits count as -inf and -inf experts are chosen last, lowest id first: every
+    id is a valid, distinct expert and the grouping stays a permutation of the pairs; a
+    token whose logits are all NaN or -inf gets weight 0 (one-CTA and split routers)."""
+    logits = W.normal_f32((m, 128), W.seed_of("route-nan", m))
+    logits[0, [1, 5, 9]] = np.nan
+    logits[1, 4:] = -np.inf
+    logits[2, :] = np.nan
+    logits[3, ::2] = -np.inf
+    logits[3, 1::4] = np.nan
+    for softmax_all in (False, True):
+        ids, probs, offsets, pairs = lib.route_topk(upload_f32(logits), 8, softmax_all=softmax_all)
+        torch.cuda.synchronize()
+        oids, oprobs = OM.route_topk(logits, 8, softmax_all)
+        _, ooffsets, opairs = OM.group_by_expert(oids, 128)
+        assert np.array_equal(ids.cpu().numpy(), oids)
+        assert np.array_equal(offsets.cpu().numpy(), ooffsets)
+        assert np.array_equal(pairs.cpu().numpy(), opairs)
+        p = probs.cpu().numpy()
+        assert np.all(np.isfinite(p))
+        assert np.all(p[oprobs == 0] == 0)
+        assert np.max(np.abs(p - oprobs)) <= 2e-5
+
+
 def test_route_ties_go_to_lower_id(lib):
     logits = np.zeros((4, 128), np.float32)
     logits[0, [3, 77, 9, 100]] = 2.0          # four-way tie at the top
@@ -79,38 +105,42 @@ def test_route_ties_go_to_lower_id(lib):
     assert ids[3, :2].tolist() == [50, 60]
 
 
-def _stack_q(mats):
-    qs = [F.quantize_matrix(w) for w in mats]
-    return np.stack([q[0] for q in qs]), np.stack([q[1] for q in qs]), np.array([q[2] for q in qs], np.float32)
-
-
 _EXPERTS = {}
 
 
 def _experts(lib, case, shared):
-    """Host fp32 expert stacks and their GPU-prepared weights, cached per shape (the
-    weights do not depend on m)."""
+    """The layer's weights quantized by the oracle (per-expert stacks and the shared
+    expert), and the same bytes repacked on the GPU for the kernels; cached per shape
+    (the weights do not depend on m).  The GPU quantizer is checked against the
+    oracle's bytes on the expert stacks on the way."""
     key = (case.d, case.inter, case.n_experts, case.tag, shared)
     if key not in _EXPERTS:
         _EXPERTS.clear()
         gu = np.stack([case.gate_up(e) for e in range(case.n_experts)])
         dn = np.stack([case.down(e) for e in range(case.n_experts)])
-        wgu = lib.prepare(upload_f32(gu), gated=True)
-        wdn = lib.prepare(upload_f32(dn))
-        sgu = sdn = None
+        qgu, qdn = F.quantize_stack(gu), F.quantize_stack(dn)
+        assert_gpu_quantizer_matches(lib, gu, qgu, f"gate_up stack {gu.shape}")
+        assert_gpu_quantizer_matches(lib, dn, qdn, f"down stack {dn.shape}")
+        del gu, dn
+        wgu = upload_oracle_weight(lib, qgu, gated=True)
+        wdn = upload_oracle_weight(lib, qdn)
+        qsgu = qsdn = sgu = sdn = None
         if shared:
-            sgu = lib.prepare(upload_f32(case.gate_up(-1)), gated=True)
-            sdn = lib.prepare(upload_f32(case.down(-1)))
-        _EXPERTS[key] = (gu, dn, wgu, wdn, sgu, sdn)
+            qsgu, qsdn = F.quantize_matrix(case.gate_up(-1)), F.quantize_matrix(case.down(-1))
+            sgu = upload_oracle_weight(lib, qsgu, gated=True)
+            sdn = upload_oracle_weight(lib, qsdn)
+        torch.cuda.synchronize()
+        _EXPERTS[key] = (qgu, qdn, qsgu, qsdn, wgu, wdn, sgu, sdn)
     return _EXPERTS[key]
 
 
 def _moe_case(lib, m, d, inter, n_exp, top_k, shared, tag, logits=None, rows=None, softmax_all=False,
               expert_scale=None):
     """Run the layer on the GPU for all m tokens; the oracle computes the tokens in
-    `rows` (all by default) -- a token's output depends on its own x and logits only."""
+    `rows` (all by default) -- a token's output depends on its own x and logits only.
+    Kernels and oracle use the same (oracle-quantized) weight bytes."""
     case = W.MoECase(m=m, d=d, inter=inter, n_experts=n_exp, top_k=top_k, tag=tag)
-    gu, dn, wgu, wdn, sgu, sdn = _experts(lib, case, shared)
+    qgu, qdn, qsgu, qsdn, wgu, wdn, sgu, sdn = _experts(lib, case, shared)
     xb, xf = case.x()
     if logits is None:
         logits = case.logits()
@@ -124,23 +154,7 @@ def _moe_case(lib, m, d, inter, n_exp, top_k, shared, tag, logits=None, rows=Non
     if rows is not None:
         rows = np.asarray(rows)
         xf, logits, got = xf[rows], logits[rows], got[rows]
-    # oracle: quantize only the experts the (sampled) routing uses, plus the shared one
-    oids, _ = OM.route_topk(logits, top_k)
-    used = sorted(set(oids.reshape(-1).tolist()))  # (the options change the weights, not the ids)
-    gq = [None] * n_exp
-    dq = [None] * n_exp
-    for e in used:
-        gq[e] = F.quantize_matrix(gu[e])
-        dq[e] = F.quantize_matrix(dn[e])
-    zero_g = (np.zeros_like(gq[used[0]][0]), np.zeros_like(gq[used[0]][1]), np.float32(0))
-    zero_d = (np.zeros_like(dq[used[0]][0]), np.zeros_like(dq[used[0]][1]), np.float32(0))
-    gq = [q if q is not None else zero_g for q in gq]
-    dq = [q if q is not None else zero_d for q in dq]
-    gate_up = (np.stack([q[0] for q in gq]), np.stack([q[1] for q in gq]), np.array([q[2] for q in gq]))
-    down = (np.stack([q[0] for q in dq]), np.stack([q[1] for q in dq]), np.array([q[2] for q in dq]))
-    sh_gu = F.quantize_matrix(case.gate_up(-1)) if shared else None
-    sh_dn = F.quantize_matrix(case.down(-1)) if shared else None
-    ref = OM.moe_layer(xf.astype(np.float64), logits, top_k, gate_up, down, sh_gu, sh_dn, softmax_all, expert_scale)
+    ref = OM.moe_layer(xf.astype(np.float64), logits, top_k, qgu, qdn, qsgu, qsdn, softmax_all, expert_scale)
     return got, ref, (ids, offsets, pairs)
 
 
@@ -199,20 +213,15 @@ def test_moe_workspace_reused_across_shapes(lib):
 
 
 def test_moe_prefill_config4_full_size(lib):
-    """The M=512 prefill chunk through the full-size layer: all 512 tokens run on the
-    GPU; the oracle checks a sample of tokens spread over the chunk (first, last and
-    seeded picks, so that their pairs fall in first, middle and ragged last blocks)."""
+    """The M=512 prefill chunk through the full-size layer: every one of the 512 tokens
+    is compared element by element with the oracle (which dequantizes each expert once
+    and applies it to the tokens routed to it), and the grouping is bit-exact."""
     m = 512
-    rng = np.random.default_rng(W.seed_of("prefill-sample", m))
-    rows = sorted(set([0, 1, m // 2, m - 1] + rng.choice(m, 4, replace=False).tolist()))
-    got, ref, (ids, offsets, pairs) = _moe_case(lib, m, W.HIDDEN, W.INTER, W.N_EXPERTS, W.TOP_K, True, "moe",
-                                                rows=rows)
-    check_bound(got, ref["out"], ref["tol_scale"], True, f"moe prefill m={m} rows={rows}")
-    # the grouping is bit-exact for the whole chunk
-    case = W.MoECase(m=m, d=W.HIDDEN, inter=W.INTER, n_experts=W.N_EXPERTS, top_k=W.TOP_K, tag="moe")
-    oids, _ = OM.route_topk(case.logits(), W.TOP_K)
-    counts, ooffsets, opairs = OM.group_by_expert(oids, W.N_EXPERTS)
-    assert np.array_equal(offsets.cpu().numpy(), ooffsets)
-    assert np.array_equal(pairs.cpu().numpy(), opairs)
-    assert counts.max() > 16          # experts span several 16-pair blocks
+    got, ref, (ids, offsets, pairs) = _moe_case(lib, m, W.HIDDEN, W.INTER, W.N_EXPERTS, W.TOP_K, True, "moe")
+    assert got.shape == (m, W.HIDDEN)
+    check_bound(got, ref["out"], ref["tol_scale"], True, f"moe prefill m={m}")
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    assert np.array_equal(offsets.cpu().numpy(), ref["offsets"])
+    assert np.array_equal(pairs.cpu().numpy(), ref["sorted_pairs"])
+    assert ref["counts"].max() > 32   # experts span several 32-pair blocks, the last one ragged
     assert lib.device_error() == 0

@@ -162,3 +162,101 @@ def test_bf16_round_matches_torch():
                         np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8)])])
     ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
     assert np.array_equal(F.bf16_round(x), ref)
+
+
+# ------------------------------------------------------------------ exact-quotient quantizer
+
+def _exact_nearest(x, grid_vals, grid_codes):
+    """Nearest grid value to the exact rational x >= 0, ties to the even code (brute force)."""
+    best, best_d = None, None
+    for v, c in zip(grid_vals, grid_codes):
+        d = abs(x - v)
+        if best_d is None or d < best_d or (d == best_d and c % 2 == 0):
+            best, best_d = c, d
+    return best
+
+
+def _quantize_brute_exact(w):
+    """The quantizer written over exact rationals: g = fp32(amax / 2688); per block the
+    E4M3 code nearest to bmax / (6 g), ties to even, saturating at 448; per element the
+    E2M1 code nearest to |w| / (e4m3(s) g), ties to even, saturating at 6, sign kept."""
+    from fractions import Fraction as Fr
+    w = np.asarray(w, np.float32)
+    n, k = w.shape
+    amax = np.max(np.abs(w))
+    g = np.float32(np.float32(amax) / np.float32(2688.0))   # one correctly rounded fp32 division
+    e4_codes = list(range(0x7F))
+    e4_vals = [Fr(float(F.e4m3_value(c))) for c in e4_codes]
+    e2_codes = list(range(8))
+    e2_vals = [Fr(float(F.e2m1_value(c))) for c in e2_codes]
+    gq = Fr(float(g))
+    sc = np.zeros((n, k // 16), np.uint8)
+    q = np.zeros((n, k), np.uint8)
+    for r in range(n):
+        for j in range(k // 16):
+            blk = [Fr(float(x)) for x in w[r, 16 * j:16 * j + 16]]
+            t = max(abs(x) for x in blk) / (6 * gq)
+            c = 0x7E if t >= 448 else _exact_nearest(t, e4_vals, e4_codes)
+            sc[r, j] = c
+            s = e4_vals[c]
+            for i, x in enumerate(blk):
+                if s == 0:
+                    continue
+                v = abs(x) / (s * gq)
+                code = 7 if v >= 6 else _exact_nearest(v, e2_vals, e2_codes)
+                q[r, 16 * j + i] = code | (8 if np.signbit(w[r, 16 * j + i]) else 0)
+    return q, sc, g
+
+
+def _near_midpoint_matrix():
+    """Blocks whose maxima, and elements, sit on or one fp32 step either side of the
+    exact rounding midpoints, under a global scale with a full 24-bit significand."""
+    amax = np.float32(1.2345678)
+    g = np.float64(np.float32(amax / np.float32(2688.0)))
+    rows = []
+    e4 = F.e4m3_value(np.arange(0x7F))
+    e2 = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    for c in (9, 30, 37, 50, 61, 77, 100, 117):          # midpoints between codes c and c + 1
+        mid = (e4[c] + e4[c + 1]) / 2 * 6 * g            # exact real bmax of the midpoint
+        for bmax in (np.nextafter(np.float32(mid), np.float32(0)), np.float32(mid),
+                     np.nextafter(np.float32(mid), np.float32(10))):
+            row = np.zeros(16, np.float32)
+            row[0] = bmax
+            # elements near E2M1 midpoints of the scale this block should get
+            s = e4[c] if bmax < mid else (e4[c + 1] if bmax > mid else e4[c + (c % 2)])
+            for i, (a, b) in enumerate(zip(e2[:-1], e2[1:])):
+                m2 = np.float32((a + b) / 2 * s * g)
+                row[1 + 2 * i] = np.nextafter(m2, np.float32(0)) if i % 2 else m2
+                row[2 + 2 * i] = -np.nextafter(m2, np.float32(10))
+            rows.append(row)
+    w = np.stack(rows)
+    w[0, 15] = amax                                       # fixes the global maximum
+    return w
+
+
+def test_quantize_matches_exact_rational_brute_force():
+    """The oracle's quantizer equals the quantizer written over exact rationals, on
+    random blocks and on blocks planted at the rounding midpoints."""
+    rng = np.random.default_rng(17)
+    rand = (0.02 * rng.standard_normal((6, 64))).astype(np.float32)
+    for w in (rand, _near_midpoint_matrix()):
+        nib, sc, g = F.quantize_matrix(w)
+        q_ref, sc_ref, g_ref = _quantize_brute_exact(w)
+        assert g == g_ref
+        assert np.array_equal(sc, sc_ref)
+        assert np.array_equal(F.unpack_nibbles(nib), q_ref)
+
+
+def test_exact_quotients_differ_from_fp32_quotients_on_planted_midpoints():
+    """The planted blocks have teeth: deciding on IEEE fp32 quotients ((bmax / 6) / g and
+    w / fp32(s * g)) picks other codes for some of them than the exact quotients."""
+    w = _near_midpoint_matrix()
+    nib, sc, g = F.quantize_matrix(w)
+    blocks = w.reshape(w.shape[0], -1, 16)
+    bmax = np.max(np.abs(blocks), axis=2).astype(np.float32)
+    t32 = (bmax / np.float32(6.0)).astype(np.float32) / g
+    sc32 = F.e4m3_encode_nonneg(t32.astype(np.float32))
+    den32 = (F.e4m3_value(sc).astype(np.float32) * g).astype(np.float32)
+    q32 = F.e2m1_encode((blocks / den32[:, :, None]).astype(np.float32)).reshape(w.shape)
+    diff = int(np.sum(sc32 != sc)) + int(np.sum(q32 != F.unpack_nibbles(nib)))
+    assert diff > 0

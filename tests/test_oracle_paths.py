@@ -91,6 +91,33 @@ def test_route_weight_options_closed_forms():
     assert np.allclose(MO.route_topk(l, 6, softmax_all=True)[1], MO.route_topk(l, 6)[1], rtol=1e-12)
 
 
+def test_route_nan_and_neginf_logits():
+    """A NaN logit counts as -inf: -inf experts are chosen after every finite one, lowest
+    id first (brute force over (value, id) with NaN read as -inf), each id is valid and
+    distinct, their weights are 0 (exp(-inf) = 0), and a token whose logits are all -inf
+    or NaN gets weight 0 on every slot (both weight readings)."""
+    rng = np.random.default_rng(8)
+    logits = rng.standard_normal((4, 16))
+    logits[0, [2, 7]] = np.nan
+    logits[1, 3:] = -np.inf                       # three finite, then the rest -inf
+    logits[2, :] = np.nan
+    logits[3, ::2] = -np.inf
+    logits[3, 1::4] = np.nan
+    for softmax_all in (False, True):
+        ids, probs = MO.route_topk(logits, 6, softmax_all)
+        for m in range(4):
+            key = np.where(np.isnan(logits[m]), -np.inf, logits[m])
+            brute = sorted(range(16), key=lambda e: (-key[e], e))[:6]
+            assert ids[m].tolist() == brute
+            assert len(set(ids[m].tolist())) == 6
+            fin = np.isfinite(key[ids[m]])
+            assert np.all(probs[m][~fin] == 0.0)
+        assert ids[1, 3:].tolist() == [3, 4, 5]
+        assert ids[2].tolist() == [0, 1, 2, 3, 4, 5] and np.all(probs[2] == 0.0)
+        # row 1: every finite logit is chosen, so both readings sum to 1
+        assert np.isclose(probs[1].sum(), 1.0, rtol=0, atol=1e-15)
+
+
 def test_grouping_brute_force():
     rng = np.random.default_rng(3)
     ids = np.stack([rng.choice(16, 4, replace=False) for _ in range(9)]).astype(np.int32)
