@@ -271,6 +271,18 @@ nvfp4_status lm_head_sample(const nvfp4_weight *w, const uint16_t *x, int32_t m,
                             float *max_key, int32_t *token, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * lm_head_sample with the final-logit softcap of TensorSharp
+ * docs/models/gemma4.md, "4.8 Logit softcap": every logit l becomes
+ * softcap * tanh(l / softcap) before the temperature and the noise (softcap 0:
+ * off, exactly lm_head_sample).  With temperature 0 this is the greedy argmax of
+ * the capped logits, max_key being the capped maximum.  softcap must be finite
+ * and >= 0 (else NVFP4_ERR_SHAPE); everything else as lm_head_sample.
+ */
+nvfp4_status lm_head_sample_ex(const nvfp4_weight *w, const uint16_t *x, int32_t m, float softcap, float temperature,
+                               uint64_t seed, float *max_key, int32_t *token, void *ws, size_t ws_bytes,
+                               cudaStream_t stream);
+
+/*
  * lm_head_argmax without a caller-provided workspace.  The pages have no
  * counterpart to this call: it exists for callers that cannot allocate device
  * memory -- for example a plugin or runtime that hands the library only its
@@ -303,14 +315,32 @@ nvfp4_status lm_head_argmax_noalloc(const nvfp4_weight *w, const uint16_t *x, in
  *            k = d), 3 MoE down (n = d, k = inter).
  *   m, top_k, n_experts  as the product's call (top_k, n_experts: MoE only).
  *   sms      the grid's SM count to plan for (the library plans for the device's).
- *   out      (host) int32 [10]: K split S, chunks per slice L, ring stages per
- *            warp, staged chunks per row, staged rows, segments one CTA may
- *            stage (decode kernel), grid, segment-list capacity, 1 if the
- *            prefill kernel runs it, dynamic shared memory bytes.
+ *   out      (host) int32 [10 or 11]: K split S, chunks per slice L, ring
+ *            stages per warp, staged chunks per row, staged rows, segments one
+ *            CTA may stage (decode kernel), grid, segment-list capacity, 1 if the
+ *            prefill kernel runs it, dynamic shared memory bytes, and (if
+ *            out_len >= 11) 1 if CTA ranges are aligned to K slices.
  * Returns NVFP4_ERR_SHAPE for shapes the product rejects or no plan fits.
  */
 nvfp4_status nvfp4_plan_info(int32_t product, int32_t m, int32_t n, int32_t k, int32_t top_k, int32_t n_experts,
                              int32_t sms, int32_t *out, int32_t out_len);
+
+/*
+ * Host-side walk of the launch a product would make (same arguments as
+ * nvfp4_plan_info) over n_seg segments, through the kernels' own work
+ * decomposition code: every CTA, run, warp and piece.  No device work and no
+ * CUDA call.
+ *   out  (host) int32 [8]: 1 if every (segment, 64-row group, 16-row tile, K
+ *        slice) is computed exactly once, every piece lies in its CTA's staged
+ *        columns and segments (a prefill piece in its run's block), and every
+ *        K-split counter in its fixed area (else 0); the largest staged column
+ *        span; the planned span capacity; the most segments one CTA stages; the
+ *        planned segment capacity; the tiles and the pieces walked; the dynamic
+ *        shared memory bytes.
+ * Returns NVFP4_ERR_SHAPE for rejected shapes or n_seg above the plan's capacity.
+ */
+nvfp4_status nvfp4_plan_check(int32_t product, int32_t m, int32_t n, int32_t k, int32_t top_k, int32_t n_experts,
+                              int32_t sms, int32_t n_seg, int32_t *out, int32_t out_len);
 
 #ifdef __cplusplus
 }

@@ -26,7 +26,7 @@ EXPORTS = (
     "nvfp4_quantize_workspace_bytes", "nvfp4_quantize", "nvfp4_repack", "nvfp4_gemm_workspace_bytes",
     "nvfp4_gemm", "moe_route_topk", "moe_ffn_workspace_bytes", "moe_ffn_grouped",
     "lm_head_workspace_bytes", "lm_head_argmax", "lm_head_argmax_noalloc", "nvfp4_plan_info",
-    "lm_head_sample", "moe_route_topk_ex",
+    "lm_head_sample", "moe_route_topk_ex", "lm_head_sample_ex", "nvfp4_plan_check",
 )
 
 
@@ -97,6 +97,11 @@ def _sig(lib):
     lib.lm_head_sample.restype = ctypes.c_int
     lib.nvfp4_plan_info.argtypes = [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int32), _I]
     lib.nvfp4_plan_info.restype = ctypes.c_int
+    lib.nvfp4_plan_check.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int32), _I]
+    lib.nvfp4_plan_check.restype = ctypes.c_int
+    lib.lm_head_sample_ex.argtypes = [ctypes.POINTER(CWeight), _P, _I, ctypes.c_float, ctypes.c_float, ctypes.c_uint64,
+                                      _P, _P, _P, _SZ, _P]
+    lib.lm_head_sample_ex.restype = ctypes.c_int
     for name in ("nvfp4_quantize", "nvfp4_repack", "nvfp4_gemm", "moe_route_topk", "moe_ffn_grouped",
                  "lm_head_argmax", "lm_head_argmax_noalloc", "nvfp4_device_error"):
         getattr(lib, name).restype = ctypes.c_int
@@ -206,17 +211,24 @@ class Library:
             _stream(stream)))
         return out
 
-    def lm_head_sample(self, w: Weight, x: torch.Tensor, temperature: float, seed: int, out=None, stream=None):
-        """Gumbel-max sample per token row: returns (max key, token)."""
+    def lm_head_sample(self, w: Weight, x: torch.Tensor, temperature: float, seed: int, out=None, stream=None,
+                       softcap: float = 0.0):
+        """Gumbel-max sample per token row (temperature 0: greedy): returns (max key, token).
+        softcap > 0 applies cap * tanh(logit / cap) to every logit first."""
         m = x.shape[0]
         if out is None:
             out = (torch.empty((m,), dtype=torch.float32, device=x.device),
                    torch.empty((m,), dtype=torch.int32, device=x.device))
         ws = self.workspace("lm_head", self.lib.lm_head_workspace_bytes(m, w.n), x.device)
         cw = w.c()
-        self._check("lm_head_sample", self.lib.lm_head_sample(
-            ctypes.byref(cw), x.data_ptr(), m, float(temperature), int(seed) & (2 ** 64 - 1), out[0].data_ptr(),
-            out[1].data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
+        if softcap:
+            self._check("lm_head_sample_ex", self.lib.lm_head_sample_ex(
+                ctypes.byref(cw), x.data_ptr(), m, float(softcap), float(temperature), int(seed) & (2 ** 64 - 1),
+                out[0].data_ptr(), out[1].data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
+        else:
+            self._check("lm_head_sample", self.lib.lm_head_sample(
+                ctypes.byref(cw), x.data_ptr(), m, float(temperature), int(seed) & (2 ** 64 - 1), out[0].data_ptr(),
+                out[1].data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
         return out
 
     def plan_lm_head_sample(self, w: Weight, x: torch.Tensor, temperature: float, seed: int, max_key, token,

@@ -2,8 +2,9 @@
 
     python -m nvfp4_w4a16_moe_skinny_gb300.build
 
-writes ``nvfp4_w4a16_moe_skinny_gb300/libnvfp4skinny.so``.  One translation
-unit, one ``-gencode`` (compute_103a -> sm_103a); no CMake.
+writes ``nvfp4_w4a16_moe_skinny_gb300/libnvfp4skinny.so``: the host unit and
+one unit per streaming epilogue, compiled in parallel (objects in ``_build/``)
+and linked; one ``-gencode`` (compute_103a -> sm_103a); no CMake.
 """
 
 from __future__ import annotations
@@ -15,7 +16,6 @@ import sys
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SRC = os.path.join(PKG, "csrc", "nvfp4_skinny.cu")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libnvfp4skinny.so")
 GENCODE = "arch=compute_103a,code=sm_103a"
@@ -26,6 +26,12 @@ def nvcc_path() -> str:
         if cand and os.path.exists(cand):
             return cand
     raise RuntimeError("nvcc not found: the CUDA 13 toolkit is required to build the library")
+
+
+def units():
+    """The translation units: the host side (nvfp4_skinny.cu) and one per streaming epilogue."""
+    csrc = os.path.join(PKG, "csrc")
+    return [os.path.join(csrc, f) for f in sorted(os.listdir(csrc)) if f.endswith(".cu")]
 
 
 def sources():
@@ -41,19 +47,33 @@ def up_to_date() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile every translation unit (in parallel) and link the shared library."""
     if not force and up_to_date():
         return LIB
-    cmd = [
-        nvcc_path(), "-gencode", GENCODE, "-O3", "-lineinfo", "-std=c++17",
-        "-I" + INCLUDE, "-Xcompiler", "-fPIC", "-shared", "-o", LIB + ".tmp", SRC,
-    ]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    res = subprocess.run(cmd, capture_output=True, text=True)
+    nvcc = nvcc_path()
+    objdir = os.path.join(PKG, "_build")
+    os.makedirs(objdir, exist_ok=True)
+    procs = []
+    for src in units():
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
+        cmd = [nvcc, "-gencode", GENCODE, "-O3", "-lineinfo", "-std=c++17", "-I" + INCLUDE, "-Xcompiler", "-fPIC",
+               "-c", "-o", obj, src]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        procs.append((obj, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)))
+    objs, errors = [], []
+    for obj, pr in procs:
+        out, err = pr.communicate()
+        if pr.returncode != 0:
+            errors.append(out + err)
+        elif verbose:
+            sys.stderr.write(err)
+        objs.append(obj)
+    if errors:
+        raise RuntimeError("nvcc failed:\n" + "\n".join(errors))
+    res = subprocess.run([nvcc, "-shared", "-o", LIB + ".tmp"] + objs, capture_output=True, text=True)
     if res.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
-    if verbose:
-        sys.stderr.write(res.stderr)
+        raise RuntimeError("link failed:\n" + res.stdout + res.stderr)
     os.replace(LIB + ".tmp", LIB)
     return LIB
 

@@ -19,10 +19,10 @@ constexpr int kTileK = 64;          // K columns per repacked tile
 constexpr int kTileBytes = 576;     // 512 B of nibbles + 64 B of scales
 constexpr int kTileNibBytes = 512;
 
-// Error word shared by all kernels of the library (read by nvfp4_device_error()).
-// Bit 0: an mbarrier wait ran out of time.  The library is one translation
-// unit, so this header is included exactly once.
-__device__ unsigned int g_device_error = 0;
+// Device error word of the kernels of one translation unit (each unit of the
+// library has its own copy; nvfp4_device_error() reads them all).  Bit 0: an
+// mbarrier wait ran out of time.
+static __device__ unsigned int g_device_error = 0;
 
 constexpr unsigned kErrWaitTimeout = 1u;
 // ~1 s at 2 GHz: far above any legitimate wait for a bulk copy.

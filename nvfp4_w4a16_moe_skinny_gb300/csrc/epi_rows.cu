@@ -1,0 +1,8 @@
+// The streaming kernels of the rows epilogue (kEpiRows): one translation unit per
+// epilogue so that the library's kernels compile in parallel.
+#include "epilogue.cuh"
+
+namespace nvfp4 {
+template nvfp4_status dispatch_stream<kEpiRows>(const Job&, const WeightMaps&, const Plan&, cudaStream_t);
+template nvfp4_status epi_error_word<kEpiRows>(uint32_t*, int);
+}  // namespace nvfp4

@@ -85,12 +85,15 @@ struct Job {
   float* max_logit;
   int* argmax;
   int ns;                 // ring stages per warp
+  int npre;               // ring stages each warp fills before waiting for the previous grid
+  int slice_ctas;         // single-segment job: CTA ranges aligned to K slices (see DecodeDeal)
   int xs_chunks;          // staged-activation capacity: chunks per row
   int xs_rows;            // staged-activation capacity: rows (plus the zero row)
   int max_cta_segs;       // segments one CTA may touch (<= kMaxCtaSegs)
   int max_segs;           // prefill kernel: capacity of the segment list
   float inv_temp;         // kEpiSample: 1 / temperature
   uint32_t seed_lo, seed_hi;  // kEpiSample: the Philox key of this call's noise
+  float softcap;          // kEpiArgmax / kEpiSample: cap of cap * tanh(logit / cap) (0: off)
 };
 
 __host__ __device__ inline size_t stream_table_bytes(int n_experts) {
@@ -112,6 +115,94 @@ __host__ __device__ inline bool deal_whole(long long nu) {
   const long long split = (4 * nu + kWarps - 1) / kWarps * 115;
   return whole <= split;
 }
+
+// Units a CTA of nu units deals whole (round-robin over its warps); the rest are
+// dealt as contiguous tile ranges.  The busiest warp's cost, whole tiles at 100
+// and split tiles at 115: all whole, ceil(nu/16) units; whole full rounds and the
+// remainder split, floor(nu/16) units + ceil(4 rem/16) tiles; all split,
+// ceil(4 nu/16) tiles.  The cheapest wins (ties to whole).
+__host__ __device__ inline int whole_units(int nu) {
+  const int full = nu / kWarps, rem = nu - full * kWarps;
+  const long long c_whole = static_cast<long long>((nu + kWarps - 1) / kWarps) * 400;
+  const long long c_hyb = static_cast<long long>(full) * 400 + static_cast<long long>((4 * rem + kWarps - 1) / kWarps) * 115;
+  const long long c_split = static_cast<long long>((4 * nu + kWarps - 1) / kWarps) * 115;
+  if (c_whole <= c_hyb && c_whole <= c_split) return nu;
+  return c_hyb <= c_split ? full * kWarps : 0;
+}
+
+__host__ __device__ constexpr int imin_(int a, int b) { return a < b ? a : b; }
+
+// One warp's share of one unit: 1 to 4 adjacent tiles of (segment, K slice,
+// 64-row group).
+struct Piece {
+  int seg, s, grp, t0, tn;
+};
+
+// The decode kernel's work decomposition, used by the kernel and by the
+// host-side plan check (nvfp4_plan_check), so both walk the same code.  Units
+// are (segment, slice, group), numbered segment-major, then slice, then group.
+// CTA b owns the contiguous units [u0, u1): a balanced share of all units, or,
+// for a single-segment job planned with slice_ctas (the grid a multiple of S),
+// a balanced share of the groups of slice b / (grid / S), so that it stages one
+// slice of K.  The CTA deals whole_units(nu) of its units whole, round-robin
+// over its warps, and the rest as contiguous tile ranges.
+struct DecodeDeal {
+  int n_seg, S, L, kc, ng, grid, slice_ctas;
+  __host__ __device__ int per_seg() const { return S * ng; }
+  __host__ __device__ void cta_range(int b, int& u0, int& u1) const {
+    if (slice_ctas && n_seg == 1 && S > 1 && grid % S == 0) {
+      const int cps = grid / S, s = b / cps, j = b % cps;
+      u0 = s * ng + static_cast<int>(static_cast<long long>(ng) * j / cps);
+      u1 = s * ng + static_cast<int>(static_cast<long long>(ng) * (j + 1) / cps);
+      return;
+    }
+    const long long n_units = static_cast<long long>(n_seg) * per_seg();
+    u0 = static_cast<int>(n_units * b / grid);
+    u1 = static_cast<int>(n_units * (b + 1) / grid);
+  }
+  __host__ __device__ int slice_len(int s) const { return imin_(kc, (s + 1) * L) - s * L; }
+  // the CTA's first segment, segment count and staged chunks [c_lo, c_hi)
+  __host__ __device__ void span(int u0, int u1, int& cseg0, int& nsc, int& c_lo, int& c_hi) const {
+    const int nu = u1 - u0;
+    cseg0 = nu > 0 ? u0 / per_seg() : 0;
+    nsc = nu > 0 ? (u1 - 1) / per_seg() - cseg0 + 1 : 0;
+    c_lo = 0, c_hi = nu > 0 ? kc : 0;
+    if (nsc == 1) {
+      c_lo = ((u0 - cseg0 * per_seg()) / ng) * L;
+      c_hi = imin_(kc, ((u1 - 1 - cseg0 * per_seg()) / ng + 1) * L);
+    }
+  }
+  // warp w's pieces of the CTA's nu units starting at u0: its whole units (units
+  // w, w+16, ... of the first whole_units(nu)), then its contiguous tile range of
+  // the remaining units
+  __host__ __device__ int n_pieces(int nu, int w) const {
+    const int nw = whole_units(nu), rest = nu - nw;
+    const int whole = nw > w ? (nw - w + kWarps - 1) / kWarps : 0;
+    const int T0 = (4 * rest * w) / kWarps, T1 = (4 * rest * (w + 1)) / kWarps;
+    return whole + (T1 > T0 ? ((T1 - 1) >> 2) - (T0 >> 2) + 1 : 0);
+  }
+  __host__ __device__ Piece piece(int u0, int nu, int w, int k) const {
+    const int nw = whole_units(nu), rest = nu - nw;
+    const int whole = nw > w ? (nw - w + kWarps - 1) / kWarps : 0;
+    int unit, t0, tn;
+    if (k < whole) {
+      unit = u0 + k * kWarps + w, t0 = 0, tn = 4;
+    } else {
+      const int kk = k - whole;
+      const int T0 = (4 * rest * w) / kWarps, T1 = (4 * rest * (w + 1)) / kWarps;
+      const int start = kk == 0 ? T0 : ((T0 >> 2) + kk) << 2;
+      const int end = imin_(T1, ((T0 >> 2) + kk + 1) << 2);
+      unit = u0 + nw + (start >> 2), t0 = start & 3, tn = end - start;
+    }
+    Piece pc;
+    pc.seg = unit / per_seg();
+    const int r = unit - pc.seg * per_seg();
+    pc.s = r / ng;
+    pc.grp = r - pc.s * ng;
+    pc.t0 = t0, pc.tn = tn;
+    return pc;
+  }
+};
 
 __device__ __forceinline__ bool better(float v, int r, float bv, int br) {
   return v > bv || (v == bv && r < br);
@@ -179,20 +270,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  const int n_seg = misc[0];
-  const int per_seg = p.S * p.ng;  // units per segment
-  const long long n_units = static_cast<long long>(n_seg) * per_seg;
-  const int u0 = static_cast<int>(n_units * blockIdx.x / gridDim.x);
-  const int u1 = static_cast<int>(n_units * (blockIdx.x + 1) / gridDim.x);
+  const DecodeDeal dd{misc[0], p.S, p.L, p.kc, p.ng, static_cast<int>(gridDim.x), p.slice_ctas};
+  int u0, u1;
+  dd.cta_range(blockIdx.x, u0, u1);
   int nu = u1 - u0;
   // this CTA's segments and K columns (chunks [c_lo, c_hi))
-  const int cseg0 = nu > 0 ? u0 / per_seg : 0;
-  const int nsc = nu > 0 ? (u1 - 1) / per_seg - cseg0 + 1 : 0;
-  int c_lo = 0, c_hi = nu > 0 ? p.kc : 0;
-  if (nsc == 1) {
-    c_lo = ((u0 - cseg0 * per_seg) / p.ng) * p.L;
-    c_hi = min(p.kc, ((u1 - 1 - cseg0 * per_seg) / p.ng + 1) * p.L);
-  }
+  int cseg0, nsc, c_lo, c_hi;
+  dd.span(u0, u1, cseg0, nsc, c_lo, c_hi);
   if (nsc > p.max_cta_segs || c_hi - c_lo > p.xs_chunks || (smem_addr(smem) & 127u)) {
     // the launch plan does not cover this CTA's share: record it and do no work
     if (threadIdx.x == 0) atomicOr(&g_device_error, kErrPlan);
@@ -205,31 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ...), or the units' tiles as contiguous ranges, whichever leaves the busiest
   // warp less work (a split tile costs ~1.15x a tile of a whole unit: its x
   // fragments and scale work are not shared by four tiles)
-  const bool whole = deal_whole(nu);
-  struct Piece {
-    int seg, s, grp, t0, tn;
-  };
-  const int T0 = (4 * nu * warp) / kWarps, T1 = (4 * nu * (warp + 1)) / kWarps;
-  const int n_pieces = whole ? (nu - warp + kWarps - 1) / kWarps
-                             : (T1 > T0 ? ((T1 - 1) >> 2) - (T0 >> 2) + 1 : 0);
-  auto piece_at = [&](int k) -> Piece {
-    int unit, t0, tn;
-    if (whole) {
-      unit = u0 + k * kWarps + warp, t0 = 0, tn = 4;
-    } else {
-      const int start = k == 0 ? T0 : ((T0 >> 2) + k) << 2;
-      const int end = min(T1, ((T0 >> 2) + k + 1) << 2);
-      unit = u0 + (start >> 2), t0 = start & 3, tn = end - start;
-    }
-    Piece pc;
-    pc.seg = unit / per_seg;
-    const int r = unit - pc.seg * per_seg;
-    pc.s = r / p.ng;
-    pc.grp = r - pc.s * p.ng;
-    pc.t0 = t0, pc.tn = tn;
-    return pc;
-  };
-  auto slice_len = [&](int s) { return min(p.kc, (s + 1) * p.L) - s * p.L; };
+  const int n_pieces = dd.n_pieces(nu, warp);
+  auto piece_at = [&](int k) -> Piece { return dd.piece(u0, nu, warp, k); };
+  auto slice_len = [&](int s) { return dd.slice_len(s); };
 
   // ---- producer (lane 0): cursor over this warp's pieces.  A whole unit (four
   // tiles) is one bulk copy of 2,304 contiguous bytes per chunk, from a source
@@ -277,13 +339,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     --prem;
   };
+  // only the first npre stages go out before the wait for the previous grid: the
+  // activation loads after the wait then queue behind few weight copies, and the
+  // rest of the ring follows them (issue_rest, called once the loads are issued)
+  const int npre = min(ns, p.npre);
   if (lane == 0)
-    for (int st = 0; st < ns; ++st) issue_next(st);
+    for (int st = 0; st < npre; ++st) issue_next(st);
+  bool rest_issued = false;
+  auto issue_rest = [&]() {
+    if (!rest_issued) {
+      rest_issued = true;
+      if (lane == 0)
+        for (int st = npre; st < ns; ++st) issue_next(st);
+    }
+  };
 
-  if (early) pdl_wait();
-  pdl_launch_dependents();
-
-  // ---- staged rows and the (segment, slot) tables
+  // ---- staged rows and the (segment, slot) tables: they depend on the routing
+  // only, so a job whose routing is complete builds them before the wait
   const int stride = (c_hi - c_lo) * kXChunkBytes + 16;
   if (threadIdx.x == 0) {
     int nrows = 0;
@@ -332,7 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     slot_row[threadIdx.x] = row;
     slot_out[threadIdx.x] = out;
   }
-  stage_rows<kMMA>(p.x, p.k, c_lo * kTileK, c_hi - c_lo, nrows, row_src, sigma, xs, stride);
+  if (early) pdl_wait();
+  pdl_launch_dependents();
+
+  stage_rows<kMMA>(p.x, p.k, c_lo * kTileK, c_hi - c_lo, nrows, row_src, sigma, xs, stride, issue_rest);
   if (threadIdx.x < nsc_used * 16) {
     const int e = seg_list[cseg0 + (threadIdx.x >> 4)];
     const float gsc = (e == kSharedSeg) ? __ldg(p.gs_sh) : (e == kDenseSeg ? __ldg(p.gs) : __ldg(p.gs + e));
@@ -369,9 +444,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if constexpr (kEpi == kEpiArgmax || kEpi == kEpiSample) {
           const int b = kMMA ? c * 2 + (i & 1) : c;
           float key = v;  // the logit, or (sampling) logit / T + the Gumbel noise of (row, token)
+          if (p.softcap > 0.f) key = p.softcap * tanhf(key / p.softcap);  // the final-logit softcap
           if constexpr (kEpi == kEpiSample)
             if (row < p.n && slot < p.m)
-              key = fmaf(v, p.inv_temp, gumbel_from_bits(philox4x32_10_word0(row, slot, p.seed_lo, p.seed_hi)));
+              key = fmaf(key, p.inv_temp, gumbel_from_bits(philox4x32_10_word0(row, slot, p.seed_lo, p.seed_hi)));
           if (key != key) key = -INFINITY;  // a NaN counts as -inf: the result is always a valid row
           if (row < p.n && better(key, row, bv[b], bi[b])) bv[b] = key, bi[b] = row;
         } else {  // kEpiGated: rows g = gate i, g+8 = up i of block rb, i = rb*8 + g

@@ -12,11 +12,12 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <vector>
 
 #include "nvfp4_skinny.h"
 #include "common.cuh"
 #include "quant.cuh"
-#include "kernel.cuh"
+#include "launch.cuh"
 #include "prefill.cuh"
 #include "moe.cuh"
 
@@ -25,7 +26,6 @@ namespace nvfp4 {
 namespace {
 
 constexpr size_t kCounterBytes = 4096;   // arrival counters at the start of a workspace
-constexpr size_t kMaxSmem = 227 * 1024;  // per-CTA opt-in limit on sm_103a
 constexpr int kMaxDevices = 64;
 
 int sm_count() {
@@ -41,7 +41,6 @@ int sm_count() {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-nvfp4_status launched() { return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -53,21 +52,6 @@ nvfp4_status check_weight(const nvfp4_weight* w, int num_matrices, uint32_t flag
   return NVFP4_OK;
 }
 
-// Allow the kernel the full opt-in shared memory, once per (kernel, device).
-template <typename K>
-cudaError_t set_smem(K kernel, size_t bytes) {
-  static std::mutex mu;
-  static std::map<std::pair<const void*, int>, bool> done;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
-  std::lock_guard<std::mutex> lock(mu);
-  if (done.count(key)) return bytes <= kMaxSmem ? cudaSuccess : cudaErrorInvalidValue;
-  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMaxSmem));
-  if (e == cudaSuccess) done[key] = true;
-  return e;
-}
-
 // ------------------------------------------------------------------ streaming-kernel plans
 // The K split S is chosen from the shapes alone, against a fixed reference
 // parallelism (152 SMs x 16 warps), so workspace sizes are host-computable and
@@ -76,11 +60,6 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 constexpr int kPlanSMs = 152;
 constexpr int kMaxSplit = 16;
 
-struct Plan {
-  int S, L, ns, xs_chunks, xs_rows, max_cta_segs, grid, max_segs;
-  bool per_run;
-  size_t smem;
-};
 
 bool use_mma(int m) { return m >= 8; }
 // accumulator floats per lane and 16-row tile (the fixup partial of one tile)
@@ -124,13 +103,18 @@ bool make_plan(int m, int S, int ng, int kc, int n_seg_max, int n_experts, bool 
     return false;
   }
   const int per_seg = S * ng;
+  // a single matrix split along K on a grid that S divides: every CTA stays inside
+  // one slice (DecodeDeal::cta_range) and stages that slice's columns only
+  const bool slice_ctas = n_seg_max == 1 && !x_by_pair && S > 1 && sms % S == 0;
   int prev_segs = -1;
   for (int grid = sms;; grid += sms) {
     const long long nu_max = (static_cast<long long>(n_seg_max) * per_seg + grid - 1) / grid;
     const int segs = static_cast<int>(std::min<long long>(n_seg_max, (nu_max + per_seg - 1) / per_seg + 1));
     if (segs > kMaxCtaSegs) continue;
     int xs_chunks = kc;
-    if (segs == 1) {
+    if (slice_ctas && grid == sms) {
+      xs_chunks = L;
+    } else if (segs == 1) {
       const long long nu_seg = std::min<long long>(nu_max, per_seg);  // units of one run
       xs_chunks = static_cast<int>(std::min<long long>(kc, ((nu_seg + ng - 1) / ng + 1) * L));
     }
@@ -138,7 +122,8 @@ bool make_plan(int m, int S, int ng, int kc, int n_seg_max, int n_experts, bool 
     for (int ns = 8; ns >= 2; --ns) {
       const size_t smem = stream_smem_bytes(xs_rows, xs_chunks, ns, n_experts);
       if (smem <= kMaxSmem) {
-        *out = Plan{S, L, ns, xs_chunks, xs_rows, std::min(segs, kMaxCtaSegs), grid, n_seg_max, per_run, smem};
+        *out = Plan{S, L, ns, xs_chunks, xs_rows, std::min(segs, kMaxCtaSegs), grid, n_seg_max, per_run, smem,
+                    slice_ctas && grid == sms};
         return true;
       }
     }
@@ -163,22 +148,17 @@ double plan_cost(int m_tokens, int ng, int n_seg, bool x_by_pair, const Plan& pl
   const long long units = static_cast<long long>(n_seg) * S * ng;
   const long long nu = (units + kPlanSMs - 1) / kPlanSMs;  // units of the busiest CTA
   const bool mma = use_mma(m);
-  long long pieces, tile_chunks;
-  double per_tc;
-  if (deal_whole(nu)) {  // whole units round-robin
-    pieces = (nu + kWarps - 1) / kWarps;
-    tile_chunks = pieces * kChunkTiles * L;
-    per_tc = mma ? 0.26 : 0.22;
-  } else {  // the units' tiles spread over the warps
-    const long long tiles = (kChunkTiles * nu + kWarps - 1) / kWarps;
-    pieces = std::min<long long>(2, tiles);
-    tile_chunks = tiles * L;
-    per_tc = mma ? 0.30 : 0.25;
-  }
+  // the busiest warp: its whole units (round-robin) and its share of the rest's tiles
+  const int nw = whole_units(static_cast<int>(nu));
+  const long long whole = (nw + kWarps - 1) / kWarps;
+  const long long split_tiles = (kChunkTiles * (nu - nw) + kWarps - 1) / kWarps;
+  const long long pieces = whole + std::min<long long>(2, split_tiles);
+  const double per_whole = mma ? 0.26 : 0.22, per_split = mma ? 0.30 : 0.25;  // us per tile-chunk
+  const double tc_time = (whole * kChunkTiles * per_whole + split_tiles * per_split) * L;
   const int rows = plan.per_run ? 16 : (x_by_pair ? m * std::min(plan.max_cta_segs, 2) : m);
-  const double span = std::min<double>(plan.xs_chunks, L * (1.0 + static_cast<double>(nu - 1) / ng));
+  const double span = plan.slice_ctas ? L : std::min<double>(plan.xs_chunks, L * (1.0 + static_cast<double>(nu - 1) / ng));
   const double t_stage = 1.0 + rows * span * kXChunkBytes / 30000.0;
-  const double t_warp = tile_chunks * per_tc;
+  const double t_warp = tc_time;
   const double t_mem = static_cast<double>(nu) * L * kStageBytes / 40000.0;  // 40 GB/s per SM
   const int v = acc_per_tile(m), batch = v >= 12 ? 1 : (v >= 8 ? 2 : 4);
   const double t_fix = S > 1 ? 1.5 * pieces + 1.5 * ((S + batch - 1) / batch) : 0.0;
@@ -311,71 +291,6 @@ bool make_maps(const nvfp4_weight* w, const nvfp4_weight* shared, WeightMaps* ou
   return true;
 }
 
-// Programmatic dependent launch (see kernel.cuh, "Launch overlap"); switched off
-// by NVFP4_PDL=0 in the environment, for comparison runs.
-bool pdl_enabled() {
-  static const bool on = [] {
-    const char* v = std::getenv("NVFP4_PDL");
-    return !(v && v[0] == '0');
-  }();
-  return on;
-}
-
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                       Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl_enabled() ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
-nvfp4_status launch_planned(void (*kernel)(Job, WeightMaps), Job p, const WeightMaps& maps, const Plan& plan,
-                            cudaStream_t stream) {
-  if (set_smem(kernel, plan.smem) != cudaSuccess) return NVFP4_ERR_CUDA;
-  p.S = plan.S;
-  p.L = plan.L;
-  p.ns = plan.ns;
-  p.xs_chunks = plan.xs_chunks;
-  p.xs_rows = plan.xs_rows;
-  p.max_cta_segs = plan.max_cta_segs;
-  p.max_segs = plan.max_segs;
-  if (launch_pdl(kernel, dim3(plan.grid), dim3(kThreads), plan.smem, stream, p, maps) != cudaSuccess)
-    return NVFP4_ERR_CUDA;
-  return launched();
-}
-
-template <int MT, bool kMMA, int kEpi>
-nvfp4_status launch_stream(const Job& p, const WeightMaps& maps, const Plan& plan, cudaStream_t stream) {
-  return launch_planned(stream_kernel<MT, kMMA, kEpi>, p, maps, plan, stream);
-}
-
-// The decode kernel for m <= 16 (specialised on m), the prefill kernel for a
-// grouped product planned with per-segment runs.
-template <int kEpi>
-nvfp4_status dispatch_stream(const Job& p, const WeightMaps& maps, const Plan& plan, cudaStream_t stream) {
-  if constexpr (kEpi == kEpiGated || kEpi == kEpiRows)
-    if (plan.per_run) return launch_planned(prefill_kernel<kEpi>, p, maps, plan, stream);
-  switch (p.m) {
-    case 1: return launch_stream<1, false, kEpi>(p, maps, plan, stream);
-    case 2: return launch_stream<2, false, kEpi>(p, maps, plan, stream);
-    case 3: return launch_stream<3, false, kEpi>(p, maps, plan, stream);
-    case 4: return launch_stream<4, false, kEpi>(p, maps, plan, stream);
-    case 5: return launch_stream<5, false, kEpi>(p, maps, plan, stream);
-    case 6: return launch_stream<6, false, kEpi>(p, maps, plan, stream);
-    case 7: return launch_stream<7, false, kEpi>(p, maps, plan, stream);
-    case 8: return launch_stream<8, true, kEpi>(p, maps, plan, stream);
-    default: return launch_stream<16, true, kEpi>(p, maps, plan, stream);
-  }
-}
-
 void set_fixup(Job* p, void* base) {
   p->fix_cnt = static_cast<unsigned*>(base);
   p->fix = reinterpret_cast<float*>(static_cast<uint8_t*>(base) + kFixCounterBytes);
@@ -422,11 +337,18 @@ nvfp4_status nvfp4_device_error(uint32_t* out, int32_t clear) {
   if (!out) return NVFP4_ERR_NULL;
   unsigned v = 0;
   if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return NVFP4_ERR_CUDA;
-  *out = v;
   if (clear) {
     const unsigned z = 0;
     if (cudaMemcpyToSymbol(g_device_error, &z, sizeof(z)) != cudaSuccess) return NVFP4_ERR_CUDA;
   }
+  // the streaming kernels' translation units, one per epilogue
+  for (auto fn : {epi_error_word<kEpiStore>, epi_error_word<kEpiArgmax>, epi_error_word<kEpiGated>,
+                  epi_error_word<kEpiRows>, epi_error_word<kEpiSample>}) {
+    uint32_t w = 0;
+    if (const nvfp4_status st = fn(&w, clear)) return st;
+    v |= w;
+  }
+  *out = v;
   return NVFP4_OK;
 }
 
@@ -514,8 +436,10 @@ namespace {
 // The lm_head never splits K: a split would put partial logits in memory.
 // The lm_head grid: greedy argmax, or (temperature > 0) the Gumbel-max sample.
 nvfp4_status lm_head_launch(const nvfp4_weight* w, const uint16_t* x, int32_t m, float* max_logit, int32_t* argmax,
-                            void* ws, cudaStream_t stream, float temperature = 0.f, uint64_t seed = 0) {
+                            void* ws, cudaStream_t stream, float temperature = 0.f, uint64_t seed = 0,
+                            float softcap = 0.f) {
   Job p = dense_job(w, x, m);
+  p.softcap = softcap;
   p.am_cnt = static_cast<unsigned*>(ws);
   p.am_val = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes);
   p.am_idx = reinterpret_cast<int*>(p.am_val + 1024 * m);
@@ -560,6 +484,20 @@ nvfp4_status lm_head_sample(const nvfp4_weight* w, const uint16_t* x, int32_t m,
   if (!aligned(ws, 16)) return NVFP4_ERR_ALIGN;
   if (sm_count() > 1024) return NVFP4_ERR_SHAPE;
   return lm_head_launch(w, x, m, max_key, token, ws, stream, temperature, seed);
+}
+
+nvfp4_status lm_head_sample_ex(const nvfp4_weight* w, const uint16_t* x, int32_t m, float softcap, float temperature,
+                               uint64_t seed, float* max_key, int32_t* token, void* ws, size_t ws_bytes,
+                               cudaStream_t stream) {
+  if (!(softcap >= 0.f) || !(softcap < INFINITY)) return NVFP4_ERR_SHAPE;
+  if (const nvfp4_status st = check_weight(w, 1, 0)) return st;
+  if (!x || !max_key || !token) return NVFP4_ERR_NULL;
+  if (m < 1 || m > 16 || !(temperature >= 0.f) || !(temperature < INFINITY)) return NVFP4_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(max_key, 4) || !aligned(token, 4)) return NVFP4_ERR_ALIGN;
+  if (!ws || ws_bytes < lm_head_workspace_bytes(m, w->n)) return NVFP4_ERR_WORKSPACE;
+  if (!aligned(ws, 16)) return NVFP4_ERR_ALIGN;
+  if (sm_count() > 1024) return NVFP4_ERR_SHAPE;
+  return lm_head_launch(w, x, m, max_key, token, ws, stream, temperature, seed, softcap);
 }
 
 }  // extern "C"
@@ -822,37 +760,120 @@ extern "C" nvfp4_status lm_head_argmax_noalloc(const nvfp4_weight* w, const uint
 }
 
 // ------------------------------------------------------------------ plan query
+namespace nvfp4 {
+namespace {
+
+// The plan a product would launch for these shapes on `sms` SMs.
+bool product_plan(int product, int m, int n, int k, int top_k, int n_experts, int sms, Plan* pl) {
+  const int ng = ceil_div(n, kGroupRows), kc = ceil_div(k, kTileK);
+  switch (product) {
+    case 0:  // dense GEMM
+      if (m > 16) return false;
+      return make_plan(m, dense_split(m, n, k), ng, kc, 1, 0, false, false, sms, pl);
+    case 1:  // lm_head
+      if (m > 16) return false;
+      return make_plan(m, 1, ng, kc, 1, 0, false, false, sms, pl);
+    case 2:    // MoE gate+up: n = 2 * inter, k = d
+    case 3: {  // MoE down: n = d, k = inter
+      if (top_k < 1 || n_experts < top_k || m > 4096 || m * top_k > 16384) return false;
+      const int d = product == 2 ? k : n, inter = product == 2 ? n / 2 : k;
+      const MoESplits sp = moe_splits(m, top_k, n_experts, d, inter, true);
+      return make_plan(m, product == 2 ? sp.s_gu : sp.s_dn, ng, kc, sp.n_seg_max, n_experts, sp.per_run,
+                       product == 3, sms, pl);
+    }
+    default:
+      return false;
+  }
+}
+
+}  // namespace
+}  // namespace nvfp4
+
 extern "C" nvfp4_status nvfp4_plan_info(int32_t product, int32_t m, int32_t n, int32_t k, int32_t top_k,
                                         int32_t n_experts, int32_t sms, int32_t* out, int32_t out_len) {
   if (!out) return NVFP4_ERR_NULL;
   if (out_len < 10 || sms < 1 || m < 1 || n < 1 || k < 16 || (k % 16)) return NVFP4_ERR_SHAPE;
-  const int ng = ceil_div(n, kGroupRows), kc = ceil_div(k, kTileK);
   Plan pl;
-  bool ok = false;
-  switch (product) {
-    case 0:  // dense GEMM
-      if (m > 16) return NVFP4_ERR_SHAPE;
-      ok = make_plan(m, dense_split(m, n, k), ng, kc, 1, 0, false, false, sms, &pl);
-      break;
-    case 1:  // lm_head
-      if (m > 16) return NVFP4_ERR_SHAPE;
-      ok = make_plan(m, 1, ng, kc, 1, 0, false, false, sms, &pl);
-      break;
-    case 2:    // MoE gate+up: n = 2 * inter, k = d
-    case 3: {  // MoE down: n = d, k = inter
-      if (top_k < 1 || n_experts < top_k || m > 4096 || m * top_k > 16384) return NVFP4_ERR_SHAPE;
-      const int d = product == 2 ? k : n, inter = product == 2 ? n / 2 : k;
-      const MoESplits sp = moe_splits(m, top_k, n_experts, d, inter, true);
-      ok = make_plan(m, product == 2 ? sp.s_gu : sp.s_dn, ng, kc, sp.n_seg_max, n_experts, sp.per_run, product == 3,
-                     sms, &pl);
-      break;
+  if (!product_plan(product, m, n, k, top_k, n_experts, sms, &pl)) return NVFP4_ERR_SHAPE;
+  const int32_t v[11] = {pl.S,    pl.L,        pl.ns,           pl.xs_chunks, pl.xs_rows, pl.max_cta_segs,
+                         pl.grid, pl.max_segs, pl.per_run ? 1 : 0, static_cast<int32_t>(pl.smem),
+                         pl.slice_ctas ? 1 : 0};
+  for (int i = 0; i < std::min<int32_t>(out_len, 11); ++i) out[i] = v[i];
+  return NVFP4_OK;
+}
+
+// Walk a product's whole launch on the host with the kernels' own decomposition
+// code (DecodeDeal / PrefillDeal) for n_seg segments.
+extern "C" nvfp4_status nvfp4_plan_check(int32_t product, int32_t m, int32_t n, int32_t k, int32_t top_k,
+                                         int32_t n_experts, int32_t sms, int32_t n_seg, int32_t* out,
+                                         int32_t out_len) {
+  if (!out) return NVFP4_ERR_NULL;
+  if (out_len < 8 || sms < 1 || m < 1 || n < 1 || k < 16 || (k % 16) || n_seg < 1) return NVFP4_ERR_SHAPE;
+  Plan pl;
+  if (!product_plan(product, m, n, k, top_k, n_experts, sms, &pl)) return NVFP4_ERR_SHAPE;
+  if (n_seg > pl.max_segs) return NVFP4_ERR_SHAPE;
+  const int ng = ceil_div(n, kGroupRows), kc = ceil_div(k, kTileK);
+  const long long cells = static_cast<long long>(n_seg) * ng * 4 * pl.S;  // (segment, group, tile, slice)
+  if (cells > (1ll << 27)) return NVFP4_ERR_SHAPE;
+  std::vector<uint8_t> seen(static_cast<size_t>(cells), 0);
+  long long bad = 0, tiles = 0, pieces = 0;
+  int max_span = 0, max_segs = 0;
+  const long long counter_cells = static_cast<long long>(kFixCounterBytes / sizeof(unsigned));
+  auto take = [&](const Piece& pc) {
+    ++pieces;
+    if (pc.tn < 1 || pc.t0 < 0 || pc.t0 + pc.tn > 4 || pc.seg < 0 || pc.seg >= n_seg || pc.grp < 0 || pc.grp >= ng ||
+        pc.s < 0 || pc.s >= pl.S)
+      return void(++bad);
+    if (pl.S > 1 && (static_cast<long long>(pc.seg) * ng + pc.grp) * 4 + pc.t0 + pc.tn > counter_cells) ++bad;
+    for (int t = pc.t0; t < pc.t0 + pc.tn; ++t) {
+      const size_t c = ((static_cast<size_t>(pc.seg) * ng + pc.grp) * 4 + t) * pl.S + pc.s;
+      if (seen[c]++) ++bad;
+      ++tiles;
     }
-    default:
-      return NVFP4_ERR_SHAPE;
+  };
+  if (!pl.per_run) {
+    const DecodeDeal dd{n_seg, pl.S, pl.L, kc, ng, pl.grid, pl.slice_ctas ? 1 : 0};
+    for (int b = 0; b < pl.grid; ++b) {
+      int u0, u1, cseg0, nsc, c_lo, c_hi;
+      dd.cta_range(b, u0, u1);
+      dd.span(u0, u1, cseg0, nsc, c_lo, c_hi);
+      max_span = std::max(max_span, c_hi - c_lo);
+      max_segs = std::max(max_segs, nsc);
+      for (int w = 0; w < kWarps; ++w)
+        for (int j = 0; j < dd.n_pieces(u1 - u0, w); ++j) {
+          const Piece pc = dd.piece(u0, u1 - u0, w, j);
+          const int c0 = pc.s * pl.L, c1 = c0 + dd.slice_len(pc.s);
+          if (c0 < c_lo || c1 > c_hi || pc.seg < cseg0 || pc.seg >= cseg0 + nsc) ++bad;  // inside the staged span
+          take(pc);
+        }
+    }
+  } else {
+    const PrefillDeal pd{n_seg, pl.S, pl.L, kc, ng, pl.grid};
+    for (int b = 0; b < pl.grid; ++b) {
+      int u0, u1;
+      pd.cta_range(b, u0, u1);
+      for (int r = 0; r < pd.n_runs(u0, u1); ++r) {
+        const int lo = pd.run_lo(u0, r), hi = pd.run_hi(u0, u1, r);
+        max_span = std::max(max_span, pd.slice_len(pd.run_slice(u0, r)));
+        max_segs = std::max(max_segs, 1);
+        for (int w = 0; w < kWarps; ++w)
+          for (int j = 0; j < pd.n_pieces(hi - lo, w); ++j) {
+            const Piece pc = pd.piece(lo, hi - lo, w, j);
+            if (pc.seg != pd.run_seg(u0, r) || pc.s != pd.run_slice(u0, r)) ++bad;  // the run's block only
+            take(pc);
+          }
+      }
+    }
   }
-  if (!ok) return NVFP4_ERR_SHAPE;
-  const int32_t v[10] = {pl.S,    pl.L,        pl.ns,           pl.xs_chunks, pl.xs_rows, pl.max_cta_segs,
-                         pl.grid, pl.max_segs, pl.per_run ? 1 : 0, static_cast<int32_t>(pl.smem)};
-  for (int i = 0; i < 10; ++i) out[i] = v[i];
+  long long missing = 0;
+  for (long long c = 0; c < cells; ++c) missing += seen[static_cast<size_t>(c)] == 0;
+  out[0] = (bad == 0 && missing == 0) ? 1 : 0;
+  out[1] = max_span;
+  out[2] = pl.xs_chunks;
+  out[3] = max_segs;
+  out[4] = pl.max_cta_segs;
+  out[5] = static_cast<int32_t>(std::min<long long>(tiles, 0x7FFFFFFF));
+  out[6] = static_cast<int32_t>(std::min<long long>(pieces, 0x7FFFFFFF));
+  out[7] = static_cast<int32_t>(pl.smem);
   return NVFP4_OK;
 }

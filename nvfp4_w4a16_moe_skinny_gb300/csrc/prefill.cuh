@@ -44,6 +44,60 @@ __host__ __device__ inline size_t prefill_smem_bytes(int xs_chunks, int ns, int 
   return ring + bars + xs + prefill_table_bytes(max_segs);
 }
 
+// The prefill kernel's work decomposition, used by the kernel and by the
+// host-side plan check (nvfp4_plan_check).  A unit is (segment, K slice, 64-row
+// group, half): two 16-row tiles.  CTA b owns [n_units*b/grid,
+// n_units*(b+1)/grid); run r is its units of (segment, slice) block b0 + r; in a
+// run, warp w takes whole units w, w+16, ... or the units' tiles as contiguous
+// ranges, whichever leaves the busiest warp less work.
+struct PrefillDeal {
+  int n_seg, S, L, kc, ng, grid;
+  __host__ __device__ int upg() const { return 2 * ng; }
+  __host__ __device__ int per_seg() const { return S * upg(); }
+  __host__ __device__ void cta_range(int b, int& u0, int& u1) const {
+    const long long n_units = static_cast<long long>(n_seg) * per_seg();
+    u0 = static_cast<int>(n_units * b / grid);
+    u1 = static_cast<int>(n_units * (b + 1) / grid);
+  }
+  __host__ __device__ int n_runs(int u0, int u1) const { return u1 > u0 ? (u1 - 1) / upg() - u0 / upg() + 1 : 0; }
+  __host__ __device__ int run_lo(int u0, int r) const { const int b = u0 / upg() + r; return b * upg() > u0 ? b * upg() : u0; }
+  __host__ __device__ int run_hi(int u0, int u1, int r) const {
+    const int e = (u0 / upg() + r + 1) * upg();
+    return e < u1 ? e : u1;
+  }
+  __host__ __device__ int run_seg(int u0, int r) const { return (u0 / upg() + r) / S; }
+  __host__ __device__ int run_slice(int u0, int r) const { return (u0 / upg() + r) - run_seg(u0, r) * S; }
+  __host__ __device__ int slice_len(int s) const { return imin_(kc, (s + 1) * L) - s * L; }
+  __host__ __device__ static bool whole(int nu) {
+    return (nu + kWarps - 1) / kWarps * 2 * 100 <= (2 * nu + kWarps - 1) / kWarps * 115;
+  }
+  __host__ __device__ int n_pieces(int nu, int w) const {
+    if (whole(nu)) return (nu - w + kWarps - 1) / kWarps;
+    const int T0 = (2 * nu * w) / kWarps, T1 = (2 * nu * (w + 1)) / kWarps;
+    return T1 > T0 ? ((T1 - 1) >> 1) - (T0 >> 1) + 1 : 0;
+  }
+  // piece k of warp w over the run's units [lo, lo + nu); t0 is the first tile (0..3) of the group
+  __host__ __device__ Piece piece(int lo, int nu, int w, int k) const {
+    int unit, t0, tn;
+    if (whole(nu)) {
+      unit = lo + k * kWarps + w, t0 = 0, tn = 2;
+    } else {
+      const int T0 = (2 * nu * w) / kWarps, T1 = (2 * nu * (w + 1)) / kWarps;
+      const int start = k == 0 ? T0 : ((T0 >> 1) + k) << 1;
+      const int end = imin_(T1, ((T0 >> 1) + k + 1) << 1);
+      unit = lo + (start >> 1), t0 = start & 1, tn = end - start;
+    }
+    Piece pc;
+    pc.seg = unit / per_seg();
+    const int r = unit - pc.seg * per_seg();
+    pc.s = r / upg();
+    const int q = r - pc.s * upg();  // 2 * group + half
+    pc.grp = q >> 1;
+    pc.t0 = 2 * (q & 1) + t0, pc.tn = tn;
+    return pc;
+  }
+};
+
 template <int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ Job p, const __grid_constant__ WeightMaps maps) {
@@ -112,62 +166,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  const int n_seg = misc[0];
-  const int upg = 2 * p.ng;         // units of one (segment, slice): two per 64-row group
-  const int per_seg = p.S * upg;    // units per segment
-  const long long n_units = static_cast<long long>(n_seg) * per_seg;
-  const int u0 = static_cast<int>(n_units * blockIdx.x / gridDim.x);
-  const int u1 = static_cast<int>(n_units * (blockIdx.x + 1) / gridDim.x);
+  const PrefillDeal pd{misc[0], p.S, p.L, p.kc, p.ng, static_cast<int>(gridDim.x)};
+  int u0, u1;
+  pd.cta_range(blockIdx.x, u0, u1);
   // run r: the CTA's units of (segment, slice) block b0 + r; its activation rows
   // are the segment's, over the slice's columns
-  const int b0 = u1 > u0 ? u0 / upg : 0;
-  const int n_blk = u1 > u0 ? (u1 - 1) / upg - b0 + 1 : 0;
-  auto run_lo = [&](int r) { return max(u0, (b0 + r) * upg); };
-  auto run_hi = [&](int r) { return min(u1, (b0 + r + 1) * upg); };
-  auto run_seg = [&](int r) { return (b0 + r) / p.S; };
-  auto run_slice = [&](int r) { return (b0 + r) - run_seg(r) * p.S; };
+  auto run_lo = [&](int r) { return pd.run_lo(u0, r); };
+  auto run_hi = [&](int r) { return pd.run_hi(u0, u1, r); };
+  auto run_seg = [&](int r) { return pd.run_seg(u0, r); };
+  auto run_slice = [&](int r) { return pd.run_slice(u0, r); };
   const bool fits = p.L <= p.xs_chunks;
   if (!fits && threadIdx.x == 0) atomicOr(&g_device_error, kErrPlan);  // the plan does not cover a slice
-  const int n_runs = fits ? n_blk : 0;
+  const int n_runs = fits ? pd.n_runs(u0, u1) : 0;
 
-  // ---- warp w's pieces of run r: whole units (2 tiles) round-robin (warp w takes
-  // units w, w+16, ...), or the units' tiles as contiguous ranges, whichever
-  // leaves the busiest warp less work
+  // ---- warp w's pieces of run r (PrefillDeal::piece)
   struct Deal {
-    int lo, nu, T0, T1, np;
-    bool whole;
+    int lo, nu, np;
   };
   auto deal_of = [&](int r) -> Deal {
     Deal d;
     d.lo = run_lo(r);
     d.nu = run_hi(r) - d.lo;
-    d.whole = (d.nu + kWarps - 1) / kWarps * 2 * 100 <= (2 * d.nu + kWarps - 1) / kWarps * 115;
-    d.T0 = (2 * d.nu * warp) / kWarps, d.T1 = (2 * d.nu * (warp + 1)) / kWarps;
-    d.np = d.whole ? (d.nu - warp + kWarps - 1) / kWarps : (d.T1 > d.T0 ? ((d.T1 - 1) >> 1) - (d.T0 >> 1) + 1 : 0);
+    d.np = pd.n_pieces(d.nu, warp);
     return d;
   };
-  struct Piece {
-    int seg, s, grp, t0, tn;  // t0: first tile (0..3) of the group
-  };
-  auto piece_at = [&](const Deal& d, int k) -> Piece {
-    int unit, t0, tn;
-    if (d.whole) {
-      unit = d.lo + k * kWarps + warp, t0 = 0, tn = 2;
-    } else {
-      const int start = k == 0 ? d.T0 : ((d.T0 >> 1) + k) << 1;
-      const int end = min(d.T1, ((d.T0 >> 1) + k + 1) << 1);
-      unit = d.lo + (start >> 1), t0 = start & 1, tn = end - start;
-    }
-    Piece pc;
-    pc.seg = unit / per_seg;
-    const int r = unit - pc.seg * per_seg;
-    pc.s = r / upg;
-    const int q = r - pc.s * upg;  // 2 * group + half
-    pc.grp = q >> 1;
-    pc.t0 = 2 * (q & 1) + t0, pc.tn = tn;
-    return pc;
-  };
-  auto slice_len = [&](int s) { return min(p.kc, (s + 1) * p.L) - s * p.L; };
+  auto piece_at = [&](const Deal& d, int k) -> Piece { return pd.piece(d.lo, d.nu, warp, k); };
+  auto slice_len = [&](int s) { return pd.slice_len(s); };
 
   // ---- producer (lane 0): cursor over this warp's pieces, run after run, ahead
   // of the consumer by the ring's depth.  A piece of tn tiles is TMA boxes of tn
@@ -207,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     --prem;
   };
   if (lane == 0)
-    for (int st = 0; st < ns; ++st) issue_next(st);
+    for (int st = 0; st < min(ns, p.npre); ++st) issue_next(st);
 
   // ---- run r's tables (thread j < 32: slot j of the segment): the source row
   // it stages (gate+up: the pair's token row of x; down: the pair's gate+up
@@ -240,12 +264,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   int c_lo = 0, stride = 16, nrows = 0;
   // after build_tables(r) and a barrier: stage run r's rows over its slice's
   // columns (ends with a barrier)
+  // the ring's stages past the first npre go out once the first run's activation
+  // loads are issued (see the decode kernel)
+  bool rest_issued = false;
+  auto issue_rest = [&]() {
+    if (!rest_issued) {
+      rest_issued = true;
+      if (lane == 0)
+        for (int st = min(ns, p.npre); st < ns; ++st) issue_next(st);
+    }
+  };
   auto stage_run = [&](int r) {
     const int nch = n_runs > 0 ? slice_len(run_slice(r)) : 0;
     c_lo = n_runs > 0 ? run_slice(r) * p.L : 0;
     stride = nch * kXChunkBytes + 16;
     nrows = n_runs > 0 ? misc[1] : 0;
-    stage_rows<true>(p.x, p.k, c_lo * kTileK, nch, nrows, row_src, sigma, xs, stride);
+    stage_rows<true>(p.x, p.k, c_lo * kTileK, nch, nrows, row_src, sigma, xs, stride, issue_rest);
   };
   if (p.routing_ready) {
     build_tables(0);

@@ -216,12 +216,14 @@ struct WeightMaps {
 // shuffles, then convert and store in the MMA fragment order or the CUDA-core
 // pair order.  Rows of up to 32*kStageRegs groups are read once and held in
 // registers; longer rows are read twice.  Columns at or past k are stored as
-// zeros.  All threads of the CTA call it; it ends with a __syncthreads.
+// zeros.  `after_loads` runs in each warp once its first row's loads are issued
+// (the caller issues the rest of its weight copies behind them; it must be safe
+// to call again).  All threads of the CTA call it; it ends with a __syncthreads.
 constexpr int kStageRegs = 12;
 
-template <bool kMMA>
+template <bool kMMA, typename F>
 __device__ __forceinline__ void stage_rows(const uint16_t* __restrict__ x, int k, int col0, int nchunks, int nrows,
-                                           const int* row_src, int* sigma, uint8_t* xs, int stride) {
+                                           const int* row_src, int* sigma, uint8_t* xs, int stride, F&& after_loads) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   const int groups = nchunks * 8;  // 8-column groups per row
@@ -269,12 +271,14 @@ __device__ __forceinline__ void stage_rows(const uint16_t* __restrict__ x, int k
     if (one_pass) {
 #pragma unroll
       for (int j = 0; j < kStageRegs; ++j) v[j] = load8(lane + 32 * j);
+      after_loads();
 #pragma unroll
       for (int j = 0; j < kStageRegs; ++j) am = fmaxf(am, amax8(v[j]));
     } else {
       for (int b = 0; b < groups; b += 32 * kStageRegs) {
 #pragma unroll
         for (int j = 0; j < kStageRegs; ++j) v[j] = load8(b + lane + 32 * j);
+        if (b == 0) after_loads();
 #pragma unroll
         for (int j = 0; j < kStageRegs; ++j) am = fmaxf(am, amax8(v[j]));
       }
@@ -298,6 +302,7 @@ __device__ __forceinline__ void stage_rows(const uint16_t* __restrict__ x, int k
       }
     }
   }
+  after_loads();
   __syncthreads();
 }
 

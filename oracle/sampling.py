@@ -74,6 +74,12 @@ def noise(rows, tokens, seed):
     return gumbel(philox4x32_10(ctr, key)[..., 0])
 
 
+def softcap_logits(logits, cap):
+    """cap * tanh(logits / cap) for cap > 0, else the logits (the same rule as router.softcap)."""
+    from .router import softcap
+    return softcap(logits, cap)
+
+
 def sample_keys(logits, temperature, seed, row0=0):
     """keys[m, n] = logits[m, n] / T + g(row0 + n, m); float64."""
     logits = np.asarray(logits, np.float64)
@@ -81,11 +87,14 @@ def sample_keys(logits, temperature, seed, row0=0):
     return logits / temperature + noise(np.arange(row0, row0 + n), np.arange(m), seed)
 
 
-def lm_head_sample(nib, scales, g, x, temperature, seed, chunk_rows: int = 8192):
+def lm_head_sample(nib, scales, g, x, temperature, seed, chunk_rows: int = 8192, softcap: float = 0.0):
     """Per token row: the index of the largest key logit/T + Gumbel noise (ties to
     the lower index), that key, the second-largest key, and tol_scale (sum|w*x| of
     the winning row, for the logit's error bound).  The logits are exact float64
-    products of the dequantized weights and x."""
+    products of the dequantized weights and x; softcap > 0 replaces each logit l
+    by softcap * tanh(l / softcap) first (TensorSharp docs/models/gemma4.md, "4.8
+    Logit softcap").  temperature 0: the key is the (capped) logit itself, no
+    noise -- the greedy argmax."""
     x = np.asarray(x, np.float64)
     m = x.shape[0]
     n = nib.shape[0]
@@ -96,7 +105,8 @@ def lm_head_sample(nib, scales, g, x, temperature, seed, chunk_rows: int = 8192)
     for lo in range(0, n, chunk_rows):
         hi = min(n, lo + chunk_rows)
         w = dequantize_matrix(nib[lo:hi], scales[lo:hi], g)
-        keys = sample_keys(x @ w.T, temperature, seed, row0=lo)
+        logits = softcap_logits(x @ w.T, softcap)
+        keys = sample_keys(logits, temperature, seed, row0=lo) if temperature > 0 else logits
         absl = np.abs(x) @ np.abs(w).T
         for t in range(m):
             row = keys[t]

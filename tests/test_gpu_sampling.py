@@ -13,20 +13,25 @@ from oracle import formats as F
 from oracle import lm_head as OLM
 from oracle import sampling as OS
 from nvfp4_w4a16_moe_skinny_gb300 import workloads as W
-from tests.gpu_helpers import upload_bf16, upload_f32
+from tests.gpu_helpers import upload_bf16, upload_f32, upload_oracle_weight
 
 pytestmark = pytest.mark.gpu
 
 NOISE_TOL = 1e-5   # fp32 -logf(-logf(u)) against float64, |g| < 17 for u in (2^-25, 1 - 2^-25)
 
 
-def _check_sample(key, tok, ref, parts, t_temp, seed, what):
+def _check_sample(key, tok, ref, parts, t_temp, seed, what, softcap=0.0):
     nib, sc, g, xf = parts
     for t in range(len(tok)):
         rows = [int(tok[t]), int(ref["index"][t])]
         lg, la = OLM.logits_rows(nib, sc, g, xf[t:t + 1].astype(np.float64), rows)
-        keys = lg[0] / t_temp + OS.noise(np.array(rows), np.array([t]), seed)[0]
-        tol = 1e-3 * max(la[0, 0], la[0, 1]) / t_temp + NOISE_TOL
+        lg = OS.softcap_logits(lg, softcap)     # the cap's slope is at most 1: the logit bound carries over
+        if t_temp > 0:
+            keys = lg[0] / t_temp + OS.noise(np.array(rows), np.array([t]), seed)[0]
+            tol = 1e-3 * max(la[0, 0], la[0, 1]) / t_temp + NOISE_TOL + 1e-6 * softcap / t_temp
+        else:
+            keys = lg[0]
+            tol = 1e-3 * max(la[0, 0], la[0, 1]) + 1e-6 * softcap
         gap = ref["key"][t] - ref["second"][t]
         if gap > 2 * tol:
             assert rows[0] == rows[1], f"{what}: token {t} sampled {rows[0]} != {rows[1]} (gap {gap:.3g})"
@@ -53,6 +58,27 @@ def test_sample_small_vocab(lib, m, t_temp):
     nib, sc, g = F.quantize_matrix(w)
     ref = OS.lm_head_sample(nib, sc, g, xf.astype(np.float64), t_temp, seed)
     _check_sample(key, tok, ref, (nib, sc, g, xf), t_temp, seed, f"sample m={m} T={t_temp}")
+    assert lib.device_error() == 0
+
+
+@pytest.mark.parametrize("m", [1, 15])
+@pytest.mark.parametrize("t_temp", [0.0, 1.0])
+def test_softcap_on_the_logits(lib, m, t_temp):
+    """The final-logit softcap (cap 30) in the lm_head epilogue: weights scaled so the
+    logits reach the cap's curved range; the greedy index, the sampled index and the
+    returned keys follow the oracle's capped logits."""
+    vocab, k, cap = 3000, 256, 30.0
+    w = W.weight((vocab, k), 5600 + m) * 25.0
+    xb, xf = W.activations((m, k), 5700 + m)
+    q = F.quantize_matrix(w)
+    wt = upload_oracle_weight(lib, q)
+    seed = 777 + m
+    key, tok = lib.lm_head_sample(wt, upload_bf16(xb), t_temp, seed, softcap=cap)
+    torch.cuda.synchronize()
+    ref = OS.lm_head_sample(*q, xf.astype(np.float64), t_temp, seed, softcap=cap)
+    assert np.max(np.abs(ref["key"])) > 0.5 * cap         # the cap bends the winning logits
+    _check_sample(key.cpu().numpy(), tok.cpu().numpy(), ref, (*q, xf), t_temp, seed,
+                  f"softcap m={m} T={t_temp}", softcap=cap)
     assert lib.device_error() == 0
 
 
