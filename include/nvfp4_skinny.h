@@ -170,6 +170,26 @@ nvfp4_status nvfp4_gemm(const nvfp4_weight *w, const uint16_t *x, int32_t m, uin
                         size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Router logits from the hidden state (TensorSharp docs/models/gemma4.md, "4.6
+ * MoE", step 2: the router matmul, an unweighted RMSNorm, then the learned
+ * per-expert scale ffn_gate_inp.scale):
+ *   raw[m, e]    = W_hat . x_m  (the NVFP4 skinny GEMM, fp32 accumulate and output)
+ *   logits[m, e] = raw[m, e] / sqrt(mean_e raw[m, e]^2 + eps) * gate_scale[e]
+ * The result feeds moe_route_topk.
+ *   w           the router weight, n = n_experts (<= 1024), k = hidden size;
+ *               num_matrices == 1, flags == 0.
+ *   x           (device) bf16 [m, w->k], 1 <= m <= 16, 16-byte aligned.
+ *   gate_scale  (device) fp32 [n_experts], or NULL for all ones.
+ *   eps         >= 0 (the pages give none; 1e-6 is the usual choice).
+ *   logits      (device) fp32 [m, n_experts].
+ *   ws          (device) nvfp4_gemm_workspace_bytes(m, n_experts, w->k) bytes,
+ *               under the same rules as nvfp4_gemm's workspace.
+ * Two launches on `stream` (the GEMM, then the normalisation).
+ */
+nvfp4_status moe_router_logits(const nvfp4_weight *w, const uint16_t *x, int32_t m, const float *gate_scale, float eps,
+                               float *logits, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * MoE router: per token m, the top_k largest logits (descending; equal logits
  * -> lower expert id) and a softmax over those top_k logits; then a stable
  * grouping of the m*top_k (token, slot) pairs by expert with no atomics.

@@ -26,7 +26,7 @@ EXPORTS = (
     "nvfp4_quantize_workspace_bytes", "nvfp4_quantize", "nvfp4_repack", "nvfp4_gemm_workspace_bytes",
     "nvfp4_gemm", "moe_route_topk", "moe_ffn_workspace_bytes", "moe_ffn_grouped",
     "lm_head_workspace_bytes", "lm_head_argmax", "lm_head_argmax_noalloc", "nvfp4_plan_info",
-    "lm_head_sample", "moe_route_topk_ex", "lm_head_sample_ex", "nvfp4_plan_check",
+    "lm_head_sample", "moe_route_topk_ex", "lm_head_sample_ex", "nvfp4_plan_check", "moe_router_logits",
 )
 
 
@@ -102,6 +102,8 @@ def _sig(lib):
     lib.lm_head_sample_ex.argtypes = [ctypes.POINTER(CWeight), _P, _I, ctypes.c_float, ctypes.c_float, ctypes.c_uint64,
                                       _P, _P, _P, _SZ, _P]
     lib.lm_head_sample_ex.restype = ctypes.c_int
+    lib.moe_router_logits.argtypes = [ctypes.POINTER(CWeight), _P, _I, _P, ctypes.c_float, _P, _P, _SZ, _P]
+    lib.moe_router_logits.restype = ctypes.c_int
     for name in ("nvfp4_quantize", "nvfp4_repack", "nvfp4_gemm", "moe_route_topk", "moe_ffn_grouped",
                  "lm_head_argmax", "lm_head_argmax_noalloc", "nvfp4_device_error"):
         getattr(lib, name).restype = ctypes.c_int
@@ -247,6 +249,19 @@ class Library:
                 raise NVFP4Error("lm_head_sample", st)
         run.keep = (cw, ws)
         return run
+
+    def router_logits(self, w: Weight, x: torch.Tensor, gate_scale: torch.Tensor = None, eps: float = 1e-6,
+                      out: torch.Tensor = None, stream=None) -> torch.Tensor:
+        """Router logits: the unweighted RMSNorm of W . x times the per-expert scale (fp32 [m, n_experts])."""
+        m = x.shape[0]
+        if out is None:
+            out = torch.empty((m, w.n), dtype=torch.float32, device=x.device)
+        ws = self.workspace("gemm", self.lib.nvfp4_gemm_workspace_bytes(m, w.n, w.k), x.device)
+        cw = w.c()
+        self._check("moe_router_logits", self.lib.moe_router_logits(
+            ctypes.byref(cw), x.data_ptr(), m, _ptr(gate_scale), float(eps), out.data_ptr(), ws.data_ptr(), ws.numel(),
+            _stream(stream)))
+        return out
 
     def route_topk(self, logits: torch.Tensor, top_k: int, out=None, stream=None, softmax_all: bool = False,
                    expert_scale: torch.Tensor = None):

@@ -75,7 +75,7 @@ struct Job {
   int routing_ready;      // 1: the routing is complete before this grid starts (read before the wait)
   uint16_t* y;            // kEpiStore: y[tok * y_ld + row];  kEpiGated: h[pair * y_ld + i]
   int y_ld;
-  float* yf;              // kEpiRows: d[pair * yf_ld + row]
+  float* yf;              // kEpiRows: d[pair * yf_ld + row]; kEpiStore: fp32 y if set (else bf16 y)
   int yf_ld;
   float* fix;             // fixup partials (S > 1)
   unsigned* fix_cnt;      // one counter per (segment, group, tile)
@@ -437,7 +437,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float v = a[c][i];
         const int row = rb * 16 + g + 8 * hrow;
         if constexpr (kEpi == kEpiStore) {
-          if ((kMMA || t4 == 0) && slot < p.m && row < p.n) p.y[static_cast<size_t>(slot) * p.y_ld + row] = f32_to_bf16_bits(v);
+          if ((kMMA || t4 == 0) && slot < p.m && row < p.n) {
+            if (p.yf)  // fp32 output (the router logits)
+              p.yf[static_cast<size_t>(slot) * p.yf_ld + row] = v;
+            else
+              p.y[static_cast<size_t>(slot) * p.y_ld + row] = f32_to_bf16_bits(v);
+          }
         } else if constexpr (kEpi == kEpiRows) {
           const int out = slot_out[sl * 16 + slot];
           if ((kMMA || t4 == 0) && out >= 0 && row < p.n) p.yf[static_cast<size_t>(out) * p.yf_ld + row] = v;

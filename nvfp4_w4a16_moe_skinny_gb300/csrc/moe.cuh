@@ -276,6 +276,25 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     group_pairs(s_ids, pairs, n_experts, s_cnt, s_wsum, offsets, sorted_pairs);
 }
 
+// Router normalisation (TensorSharp docs/models/gemma4.md, "4.6 MoE", step 2):
+// logits[t, e] = raw[t, e] / sqrt(mean_e raw[t, e]^2 + eps) * scale[e], in place,
+// one warp per token; the mean of squares is summed in fp32 in a fixed order
+// (lanes, then a shuffle tree).  scale == nullptr: all ones.
+__global__ void moe_router_norm_kernel(float* __restrict__ logits, int m, int n_experts,
+                                       const float* __restrict__ scale, float eps) {
+  pdl_wait();  // the raw logits come from the previous grid
+  pdl_launch_dependents();
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= m) return;
+  float* row = logits + static_cast<size_t>(t) * n_experts;
+  float ss = 0.f;
+  for (int e = lane; e < n_experts; e += 32) ss = fmaf(row[e], row[e], ss);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const float inv = rsqrtf(ss / static_cast<float>(n_experts) + eps);
+  for (int e = lane; e < n_experts; e += 32) row[e] = row[e] * inv * (scale ? __ldg(scale + e) : 1.f);
+}
+
 // out[t, j] = bf16( sum_r probs[t, r] * d[t*top_k + r, j] + d[m*top_k + t, j] ), fixed order.
 __global__ void moe_combine_kernel(const float* __restrict__ d, const float* __restrict__ probs, int m, int top_k,
                                    int cols, bool shared, uint16_t* __restrict__ out) {

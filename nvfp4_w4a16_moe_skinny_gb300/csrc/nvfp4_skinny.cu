@@ -423,6 +423,32 @@ nvfp4_status nvfp4_gemm(const nvfp4_weight* w, const uint16_t* x, int32_t m, uin
   return dispatch_stream<kEpiStore>(p, maps, plan, stream);
 }
 
+nvfp4_status moe_router_logits(const nvfp4_weight* w, const uint16_t* x, int32_t m, const float* gate_scale, float eps,
+                               float* logits, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (const nvfp4_status st = check_weight(w, 1, 0)) return st;
+  if (!x || !logits) return NVFP4_ERR_NULL;
+  if (m < 1 || m > 16 || w->n > 1024 || !(eps >= 0.f) || !(eps < INFINITY)) return NVFP4_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(logits, 4) || (gate_scale && !aligned(gate_scale, 4))) return NVFP4_ERR_ALIGN;
+  if (!ws || ws_bytes < nvfp4_gemm_workspace_bytes(m, w->n, w->k)) return NVFP4_ERR_WORKSPACE;
+  if (!aligned(ws, 16)) return NVFP4_ERR_ALIGN;
+  // the router matmul (the skinny GEMM with fp32 output), then the normalisation
+  Job p = dense_job(w, x, m);
+  p.yf = logits;
+  p.yf_ld = w->n;
+  set_fixup(&p, ws);
+  Plan plan;
+  if (!make_plan(m, dense_split(m, w->n, w->k), p.ng, p.kc, 1, 0, false, false, std::max(1, sm_count()), &plan))
+    return NVFP4_ERR_SHAPE;
+  WeightMaps maps;
+  if (!make_maps(w, nullptr, &maps)) return NVFP4_ERR_CUDA;
+  if (const nvfp4_status st = dispatch_stream<kEpiStore>(p, maps, plan, stream)) return st;
+  constexpr int kWarpsPerCta = 4;
+  if (launch_pdl(moe_router_norm_kernel, dim3(ceil_div(m, kWarpsPerCta)), dim3(32 * kWarpsPerCta), 0, stream, logits,
+                 static_cast<int>(m), static_cast<int>(w->n), gate_scale, eps) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  return launched();
+}
+
 size_t lm_head_workspace_bytes(int32_t m, int32_t vocab) {
   if (m < 1 || m > 16 || vocab < 1) return 0;
   return kCounterBytes + static_cast<size_t>(1024) * m * (sizeof(float) + sizeof(int));

@@ -113,6 +113,15 @@ def test_lm_head_and_moe_argument_errors(so):
     assert so.lm_head_sample(ctypes.byref(w), p, 1, float("nan"), 7, p, p, p, 1 << 20, None) == 2
     assert so.lm_head_sample(ctypes.byref(w), p, 1, float("inf"), 7, p, p, p, 1 << 20, None) == 2
     assert so.lm_head_sample(ctypes.byref(w), p, 1, 1.0, 7, p, p, p, 8, None) == 4
+    # the softcapped sampling lm_head: the cap must be finite and >= 0
+    assert so.lm_head_sample_ex(ctypes.byref(w), p, 1, -1.0, 1.0, 7, p, p, p, 1 << 20, None) == 2
+    assert so.lm_head_sample_ex(ctypes.byref(w), p, 1, float("inf"), 1.0, 7, p, p, p, 1 << 20, None) == 2
+    assert so.lm_head_sample_ex(ctypes.byref(w), p, 1, 30.0, 1.0, 7, None, p, p, 1 << 20, None) == 1
+    # the router logits: m <= 16, eps >= 0, the GEMM's workspace
+    assert so.moe_router_logits(ctypes.byref(w), p, 17, None, 1e-6, p, p, 1 << 20, None) == 2
+    assert so.moe_router_logits(ctypes.byref(w), p, 1, None, -1.0, p, p, 1 << 20, None) == 2
+    assert so.moe_router_logits(ctypes.byref(w), None, 1, None, 1e-6, p, p, 1 << 20, None) == 1
+    assert so.moe_router_logits(ctypes.byref(w), p, 1, None, 1e-6, p, p, 8, None) == 4
     assert so.moe_route_topk(p, 15, 128, 0, p, p, p, p, None) == 2           # top_k < 1
     assert so.moe_route_topk(p, 15, 4, 8, p, p, p, p, None) == 2             # top_k > n_experts
     assert so.moe_route_topk(p, 15, 2048, 8, p, p, p, p, None) == 2          # n_experts > 1024
