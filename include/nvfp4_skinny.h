@@ -264,7 +264,13 @@ nvfp4_status moe_ffn_grouped(const uint16_t *x, int32_t m, int32_t top_k, const 
  *   w          num_matrices == 1, flags == 0 (n = vocabulary size).
  *   x          (device) bf16 [m, w->k], 1 <= m <= 16, 16-byte aligned.
  *   max_logit  (device) fp32 [m];  argmax (device) int32 [m].
- *   ws         (device) lm_head_workspace_bytes(m, n) bytes, 8-byte aligned.
+ *   ws         (device) lm_head_workspace_bytes(m, n) bytes (4 KiB: an arrival
+ *              counter and one packed (value, row) maximum per token), 16-byte
+ *              aligned.  It must be zero before the first call on it (for
+ *              example cudaMemsetAsync once after allocation); every completed
+ *              call leaves it zero again.  The per-CTA maxima are combined with
+ *              64-bit atomic maxima on (value, inverted row), so the result does
+ *              not depend on the order the CTAs finish in.
  * A NaN logit counts as -inf, so the index is always a valid row: a token whose
  * logits are all NaN gets (-inf, 0).
  */
@@ -311,19 +317,20 @@ nvfp4_status lm_head_sample_ex(const nvfp4_weight *w, const uint16_t *x, int32_t
  * in the middle of a request.
  *
  * Same arguments, result and limits as lm_head_argmax, minus ws/ws_bytes.  The
- * scratch it needs (arrival counter + per-CTA partials, 135,168 bytes) is a
- * static array inside this library's device code, so every GPU that loads the
- * library holds it until the process exits.  No call allocates or frees memory.
+ * scratch it needs (an arrival counter and the per-token packed maxima, 4,096
+ * bytes) is a static array inside this library's device code, so every GPU that
+ * loads the library holds it until the process exits.  No call allocates or
+ * frees memory.
  *   - The first call on a device, with that device current, looks up the
  *     array's device address with cudaGetSymbolAddress and zeroes it
  *     (synchronously); make that first call before any stream capture.
  *   - Every call clears the arrival counter on `stream` before its kernel; the
- *     rest of the array keeps the last call's contents.
+ *     kernel's last CTA leaves the maxima zero for the next call.
  *   - All calls on a device share the one array: calls that may overlap on the
  *     GPU (other streams, other host threads) race and give wrong results.
  *     Serialise them, or use lm_head_argmax with separate workspaces.
  *   - Returns NVFP4_ERR_WORKSPACE if lm_head_workspace_bytes(m, w->n) exceeds
- *     the array (never for m <= 16 on a GPU with at most 1024 SMs).
+ *     the array (never for m <= 16).
  */
 nvfp4_status lm_head_argmax_noalloc(const nvfp4_weight *w, const uint16_t *x, int32_t m, float *max_logit,
                                     int32_t *argmax, cudaStream_t stream);

@@ -79,8 +79,7 @@ struct Job {
   int yf_ld;
   float* fix;             // fixup partials (S > 1)
   unsigned* fix_cnt;      // one counter per (segment, group, tile)
-  float* am_val;          // kEpiArgmax: per-CTA partial results [grid][m]
-  int* am_idx;
+  unsigned long long* am_key;  // kEpiArgmax / kEpiSample: per-token packed (value, row) maxima [m]
   unsigned* am_cnt;
   float* max_logit;
   int* argmax;
@@ -98,7 +97,7 @@ struct Job {
 
 __host__ __device__ inline size_t stream_table_bytes(int n_experts) {
   return static_cast<size_t>(4) * (kMaxStagedRows + (kMaxStagedRows + 1) + kMaxCtaSegs * 16 * 3 +
-                                   kWarps * 16 * 2 + kWarps * 8 + n_experts + 2 + 4);
+                                   kWarps * 16 * 2 + kWarps * 8 + n_experts + 2 + 4 + n_experts + 1);
 }
 
 __host__ __device__ inline size_t stream_smem_bytes(int xs_rows, int xs_chunks, int ns, int n_experts) {
@@ -116,19 +115,13 @@ __host__ __device__ inline bool deal_whole(long long nu) {
   return whole <= split;
 }
 
-// Units a CTA of nu units deals whole (round-robin over its warps); the rest are
-// dealt as contiguous tile ranges.  The busiest warp's cost, whole tiles at 100
-// and split tiles at 115: all whole, ceil(nu/16) units; whole full rounds and the
-// remainder split, floor(nu/16) units + ceil(4 rem/16) tiles; all split,
-// ceil(4 nu/16) tiles.  The cheapest wins (ties to whole).
-__host__ __device__ inline int whole_units(int nu) {
-  const int full = nu / kWarps, rem = nu - full * kWarps;
-  const long long c_whole = static_cast<long long>((nu + kWarps - 1) / kWarps) * 400;
-  const long long c_hyb = static_cast<long long>(full) * 400 + static_cast<long long>((4 * rem + kWarps - 1) / kWarps) * 115;
-  const long long c_split = static_cast<long long>((4 * nu + kWarps - 1) / kWarps) * 115;
-  if (c_whole <= c_hyb && c_whole <= c_split) return nu;
-  return c_hyb <= c_split ? full * kWarps : 0;
-}
+// Units a CTA of nu units deals whole (round-robin over its warps); the rest
+// are dealt as contiguous tile ranges.  All whole when the busiest warp's cost
+// (whole tiles at 100, split tiles at 115) is no higher than all split; else
+// all split.  (Whole full rounds with the remainder split balance the warps
+// better but measured slower at M = 15: the SM's issue slots, not the busiest
+// warp, bound the tile loop there, and split tiles cost more instructions.)
+__host__ __device__ inline int whole_units(int nu) { return deal_whole(nu) ? nu : 0; }
 
 __host__ __device__ constexpr int imin_(int a, int b) { return a < b ? a : b; }
 
@@ -208,6 +201,23 @@ __device__ __forceinline__ bool better(float v, int r, float bv, int br) {
   return v > bv || (v == bv && r < br);
 }
 
+// (value, row) as one unsigned 64-bit key whose order is `better`'s: the fp32 bits
+// made order-preserving as unsigned (sign bit flipped for non-negative values,
+// all bits inverted for negative ones) above the inverted row.  Never 0 for a
+// finite or infinite value, so 0 is below every key.
+__device__ __forceinline__ unsigned long long pack_value_row(float v, int row) {
+  const uint32_t u = __float_as_uint(v);
+  const uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<unsigned long long>(k) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(row));
+}
+__device__ __forceinline__ float unpack_value(unsigned long long key) {
+  const uint32_t k = static_cast<uint32_t>(key >> 32);
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+__device__ __forceinline__ int unpack_row(unsigned long long key) {
+  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+}
+
 __device__ __forceinline__ float gelu_tanh(float z) {
   // 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))
   const float u = 0.7978845608028654f * fmaf(0.044715f * z, z * z, z);
@@ -242,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* cur = red_i + kWarps * 16 + warp * 8;                                 // [kWarps * 8] box cursors
   int* seg_list = red_i + kWarps * 16 + kWarps * 8;                          // [n_experts + 2]
   int* misc = seg_list + p.n_experts + 2;  // [0] segments, [1] last-arrival flag, [2] staged rows
+  int* s_off = misc + 4;                   // [n_experts + 1] the expert offsets (MoE)
 
   if (lane == 0) {
     for (int s = 0; s < ns; ++s) mbar_init(&bar[s], 1);
@@ -255,18 +266,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!early) pdl_wait();
   if (dense) {
     if (threadIdx.x == 0) seg_list[0] = kDenseSeg, misc[0] = 1;
-  } else if (warp == 0) {
-    int n = 0;
-    for (int base = 0; base < p.n_experts; base += 32) {
-      const int e = base + lane;
-      const bool act = e < p.n_experts && __ldg(p.offsets + e + 1) > __ldg(p.offsets + e);
-      const uint32_t mask = __ballot_sync(0xffffffffu, act);
-      if (act) seg_list[n + __popc(mask & ((1u << lane) - 1u))] = e;
-      n += __popc(mask);
-    }
-    if (lane == 0) {
-      if (p.has_shared) seg_list[n++] = kSharedSeg;
-      misc[0] = n;
+  } else {
+    // the offsets go to shared memory in one round of loads (one per thread), then
+    // warp 0 lists the experts that received pairs
+    for (int e = threadIdx.x; e <= p.n_experts; e += blockDim.x) s_off[e] = __ldg(p.offsets + e);
+    __syncthreads();
+    if (warp == 0) {
+      int n = 0;
+      for (int base = 0; base < p.n_experts; base += 32) {
+        const int e = base + lane;
+        const bool act = e < p.n_experts && s_off[e + 1] > s_off[e];
+        const uint32_t mask = __ballot_sync(0xffffffffu, act);
+        if (act) seg_list[n + __popc(mask & ((1u << lane) - 1u))] = e;
+        n += __popc(mask);
+      }
+      if (lane == 0) {
+        if (p.has_shared) seg_list[n++] = kSharedSeg;
+        misc[0] = n;
+      }
     }
   }
   __syncthreads();
@@ -357,26 +374,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- staged rows and the (segment, slot) tables: they depend on the routing
   // only, so a job whose routing is complete builds them before the wait
   const int stride = (c_hi - c_lo) * kXChunkBytes + 16;
-  if (threadIdx.x == 0) {
-    int nrows = 0;
-    if (!p.x_by_pair) {
-      nrows = nsc_used ? p.m : 0;
-      for (int j = 0; j < nrows; ++j) row_src[j] = j;
-    } else {
-      for (int i = 0; i < nsc_used; ++i) {
-        const int e = seg_list[cseg0 + i];
-        if (e == kSharedSeg) {
-          for (int j = 0; j < p.m; ++j) row_src[nrows++] = p.m * p.top_k + j;
-        } else {
-          const int o = __ldg(p.offsets + e), cnt = min(p.m, __ldg(p.offsets + e + 1) - o);
-          for (int j = 0; j < cnt; ++j) row_src[nrows++] = __ldg(p.pairs + o + j);
-        }
-      }
-    }
-    misc[2] = nrows;
+  // staged rows of local segment i: the m tokens (dense, gate+up: one copy for
+  // all segments) or, for the down product, the segment's pairs' rows
+  auto seg_rows = [&](int i) {
+    const int e = seg_list[cseg0 + i];
+    return e < 0 ? p.m : min(p.m, s_off[e + 1] - s_off[e]);
+  };
+  int nrows = 0;
+  if (!p.x_by_pair) {
+    nrows = nsc_used ? p.m : 0;
+    for (int j = threadIdx.x; j < nrows; j += blockDim.x) row_src[j] = j;
+  } else {
+    for (int i = 0; i < nsc_used; ++i) nrows += seg_rows(i);
   }
-  __syncthreads();
-  const int nrows = misc[2];
   if (threadIdx.x < nsc_used * 16) {
     const int i = threadIdx.x >> 4, j = threadIdx.x & 15;
     const int e = seg_list[cseg0 + i];
@@ -387,23 +397,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // first staged row of segment i (down product: rows are per segment)
       int base = 0;
       if (p.x_by_pair)
-        for (int ii = 0; ii < i; ++ii) {
-          const int ee = seg_list[cseg0 + ii];
-          base += ee == kSharedSeg ? p.m : min(p.m, __ldg(p.offsets + ee + 1) - __ldg(p.offsets + ee));
-        }
+        for (int ii = 0; ii < i; ++ii) base += seg_rows(ii);
       if (e == kSharedSeg) {
         if (j < p.m) out = p.m * p.top_k + j, row = p.x_by_pair ? base + j : j;
       } else {
-        const int o = __ldg(p.offsets + e), cnt = min(p.m, __ldg(p.offsets + e + 1) - o);
+        const int o = s_off[e], cnt = min(p.m, s_off[e + 1] - o);
         if (j < cnt) {
           out = __ldg(p.pairs + o + j);
           row = p.x_by_pair ? base + j : out / p.top_k;
         }
       }
+      if (p.x_by_pair && row < nrows) row_src[row] = out;
     }
     slot_row[threadIdx.x] = row;
     slot_out[threadIdx.x] = out;
   }
+  __syncthreads();
   if (early) pdl_wait();
   pdl_launch_dependents();
 
@@ -690,15 +699,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kMMA ? g == 0 : lane == 0) red_v[warp * 16 + slot] = v, red_i[warp * 16 + slot] = rw;
     }
     __syncthreads();
-    // ---- warps -> CTA, fixed order
+    // ---- warps -> CTA, fixed order, then CTAs -> grid: one 64-bit atomic max per
+    // token on (orderable value, inverted row), whose maximum is the largest value
+    // and, among equal values, the lowest row: the result does not depend on the
+    // order the CTAs arrive in.  The last CTA to arrive reads and resets the keys.
     if (threadIdx.x < p.m) {
       const int tok = threadIdx.x;
       float v = -INFINITY;
       int rw = 0x7FFFFFFF;
       for (int w = 0; w < kWarps; ++w)
         if (better(red_v[w * 16 + tok], red_i[w * 16 + tok], v, rw)) v = red_v[w * 16 + tok], rw = red_i[w * 16 + tok];
-      p.am_val[static_cast<size_t>(blockIdx.x) * p.m + tok] = v;
-      p.am_idx[static_cast<size_t>(blockIdx.x) * p.m + tok] = rw;
+      if (rw != 0x7FFFFFFF) atomicMax(p.am_key + tok, pack_value_row(v, rw));
     }
     __threadfence();
     __syncthreads();
@@ -709,36 +720,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       misc[1] = last;
     }
     __syncthreads();
-    if (misc[1] && warp < p.m) {
-      // the last CTA: warp t reduces token t over every CTA's partial, lanes
-      // taking CTAs lane, lane+32, ... (loads in flight together), then shuffles
+    if (misc[1] && threadIdx.x < p.m) {
       __threadfence();
-      const int tok = warp;
-      float v = -INFINITY;
-      int rw = 0x7FFFFFFF;
-      for (unsigned b0 = 0; b0 < gridDim.x; b0 += 128) {
-        float ov[4];
-        int orow[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const unsigned b = b0 + 32 * j + lane;
-          ov[j] = -INFINITY, orow[j] = 0x7FFFFFFF;
-          if (b < gridDim.x) {
-            ov[j] = __ldcg(p.am_val + static_cast<size_t>(b) * p.m + tok);
-            orow[j] = __ldcg(p.am_idx + static_cast<size_t>(b) * p.m + tok);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (better(ov[j], orow[j], v, rw)) v = ov[j], rw = orow[j];
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, v, off);
-        const int orow = __shfl_xor_sync(0xffffffffu, rw, off);
-        if (better(ov, orow, v, rw)) v = ov, rw = orow;
-      }
-      if (lane == 0) p.max_logit[tok] = v, p.argmax[tok] = rw;
+      const unsigned long long key = atomicExch(p.am_key + threadIdx.x, 0ull);
+      p.max_logit[threadIdx.x] = unpack_value(key);
+      p.argmax[threadIdx.x] = unpack_row(key);
     }
   }
 }

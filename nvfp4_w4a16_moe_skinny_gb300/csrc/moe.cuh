@@ -42,35 +42,36 @@ __device__ __forceinline__ void token_topk(const float* __restrict__ logits, int
                                            const float* __restrict__ escale) {
   {
     const float* row = logits + static_cast<size_t>(t) * n_experts;
-    float lv[NPER];  // experts lane + 32*i, read once; a NaN logit counts as -inf
+    // experts lane + 32*i, read once, as 64-bit keys (pack_value_row: larger logit,
+    // then lower id, is larger); a NaN logit counts as -inf; 0 (below every valid
+    // key) marks an expert that does not exist or was already chosen
+    float lv[NPER];
+    unsigned long long key[NPER];
 #pragma unroll
     for (int i = 0; i < NPER; ++i) {
       const int e = lane + 32 * i;
       const float v = e < n_experts ? __ldg(row + e) : -INFINITY;
       lv[i] = v == v ? v : -INFINITY;
+      key[i] = e < n_experts ? pack_value_row(lv[i], e) : 0ull;
     }
-    // Every valid logit is >= -inf, so each round's winner is a valid expert not
-    // chosen before (top_k <= n_experts): when all that remain are -inf, the lowest
-    // such id.
-    uint32_t taken = 0;  // bit i: expert lane + 32*i already chosen
+    // top_k rounds of a warp-wide maximum: each round's winner is a valid expert not
+    // chosen before (top_k <= n_experts): when all that remain are -inf, the lowest id
     float myv = -INFINITY;
     int mye = 0;
     for (int r = 0; r < top_k; ++r) {
-      float bv = -INFINITY;
-      int be = 0x7FFFFFFF;
+      unsigned long long best = 0ull;
 #pragma unroll
-      for (int i = 0; i < NPER; ++i) {
-        const int e = lane + 32 * i;
-        if (e < n_experts && !((taken >> i) & 1u) && (lv[i] > bv || (lv[i] == bv && e < be))) bv = lv[i], be = e;
-      }
+      for (int i = 0; i < NPER; ++i) best = key[i] > best ? key[i] : best;
+      unsigned long long wmax = best;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (ov > bv || (ov == bv && oe < be)) bv = ov, be = oe;
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, wmax, off);
+        wmax = o > wmax ? o : wmax;
       }
-      if (lane == (be & 31)) taken |= 1u << (be >> 5);
-      if (lane == r) myv = bv, mye = be;
+#pragma unroll
+      for (int i = 0; i < NPER; ++i)
+        if (key[i] == wmax) key[i] = 0ull;  // keys are distinct: only the winner matches
+      if (lane == r) myv = unpack_value(wmax), mye = unpack_row(wmax);
     }
     // softmax over the chosen logits, or over all of them (round 0 holds the maximum);
     // a token whose logits are all -inf (or NaN) gets weight 0 on every slot
@@ -93,6 +94,54 @@ __device__ __forceinline__ void token_topk(const float* __restrict__ logits, int
       probs[t * top_k + lane] = pr;
       if (s_ids) s_ids[t * top_k + lane] = mye;
     }
+  }
+}
+
+// The stable counting sort of the pairs by expert by one warp (a decode batch:
+// few pairs): per-expert counts from batches of 32 pairs (lanes holding the same
+// expert find each other with a match; the group's first lane adds), an
+// exclusive scan of the counts (each lane a contiguous run of experts), then the
+// placement in the same batch order -- ascending pair order within an expert.
+// No atomics, no block-wide barrier.  s_cnt: scratch of n_experts ints.
+__device__ __forceinline__ void group_pairs_warp(const int* s_ids, int pairs, int n_experts, int* s_cnt, int lane,
+                                                 int* __restrict__ offsets, int* __restrict__ sorted_pairs) {
+  for (int e = lane; e < n_experts; e += 32) s_cnt[e] = 0;
+  __syncwarp();
+  for (int base = 0; base < pairs; base += 32) {
+    const int q = base + lane;
+    const int e = q < pairs ? s_ids[q] : -1 - lane;  // a lane past the end matches nobody
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    if (q < pairs && lane == __ffs(same) - 1) s_cnt[e] += __popc(same);
+    __syncwarp();
+  }
+  // exclusive scan: lane l owns experts [l*per, (l+1)*per)
+  const int per = (n_experts + 31) / 32;
+  const int e0 = min(n_experts, lane * per), e1 = min(n_experts, e0 + per);
+  int tot = 0;
+  for (int e = e0; e < e1; ++e) tot += s_cnt[e];
+  int incl = tot;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  int run = incl - tot;
+  for (int e = e0; e < e1; ++e) {
+    const int c = s_cnt[e];
+    offsets[e] = run;
+    s_cnt[e] = run;  // now the next position of expert e
+    run += c;
+  }
+  if (lane == 31) offsets[n_experts] = pairs;
+  __syncwarp();
+  for (int base = 0; base < pairs; base += 32) {
+    const int q = base + lane;
+    const int e = q < pairs ? s_ids[q] : -1 - lane;
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    if (q < pairs) sorted_pairs[s_cnt[e] + __popc(same & ((1u << lane) - 1u))] = q;
+    __syncwarp();
+    if (q < pairs && lane == __ffs(same) - 1) s_cnt[e] += __popc(same);
+    __syncwarp();
   }
 }
 
@@ -239,8 +288,9 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   for (int t = warp; t < m; t += nwarps)
     token_topk<NPER>(logits, t, n_experts, top_k, lane, ids, probs, s_ids, flags, escale);
   __syncthreads();
-  // (at most 32 tokens: the ballot sort; the histogram passes cost more here)
-  group_pairs(s_ids, pairs, n_experts, s_cnt, s_wsum, offsets, sorted_pairs);
+  // at most 32 tokens: one warp groups the pairs
+  if (warp == 0) group_pairs_warp(s_ids, pairs, n_experts, s_cnt, lane, offsets, sorted_pairs);
+  (void)s_wsum;
 }
 
 // A prefill chunk, step 1: the top-k of every token, one warp per token over

@@ -451,7 +451,7 @@ nvfp4_status moe_router_logits(const nvfp4_weight* w, const uint16_t* x, int32_t
 
 size_t lm_head_workspace_bytes(int32_t m, int32_t vocab) {
   if (m < 1 || m > 16 || vocab < 1) return 0;
-  return kCounterBytes + static_cast<size_t>(1024) * m * (sizeof(float) + sizeof(int));
+  return kCounterBytes;  // the arrival counter and the per-token packed maxima
 }
 
 }  // extern "C"
@@ -467,8 +467,7 @@ nvfp4_status lm_head_launch(const nvfp4_weight* w, const uint16_t* x, int32_t m,
   Job p = dense_job(w, x, m);
   p.softcap = softcap;
   p.am_cnt = static_cast<unsigned*>(ws);
-  p.am_val = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes);
-  p.am_idx = reinterpret_cast<int*>(p.am_val + 1024 * m);
+  p.am_key = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + 64);
   p.max_logit = max_logit;
   p.argmax = argmax;
   Plan plan;
@@ -496,7 +495,6 @@ nvfp4_status lm_head_argmax(const nvfp4_weight* w, const uint16_t* x, int32_t m,
   if (!aligned(x, 16) || !aligned(max_logit, 4) || !aligned(argmax, 4)) return NVFP4_ERR_ALIGN;
   if (!ws || ws_bytes < lm_head_workspace_bytes(m, w->n)) return NVFP4_ERR_WORKSPACE;
   if (!aligned(ws, 16)) return NVFP4_ERR_ALIGN;
-  if (sm_count() > 1024) return NVFP4_ERR_SHAPE;
   return lm_head_launch(w, x, m, max_logit, argmax, ws, stream);
 }
 
@@ -508,7 +506,6 @@ nvfp4_status lm_head_sample(const nvfp4_weight* w, const uint16_t* x, int32_t m,
   if (!aligned(x, 16) || !aligned(max_key, 4) || !aligned(token, 4)) return NVFP4_ERR_ALIGN;
   if (!ws || ws_bytes < lm_head_workspace_bytes(m, w->n)) return NVFP4_ERR_WORKSPACE;
   if (!aligned(ws, 16)) return NVFP4_ERR_ALIGN;
-  if (sm_count() > 1024) return NVFP4_ERR_SHAPE;
   return lm_head_launch(w, x, m, max_key, token, ws, stream, temperature, seed);
 }
 
@@ -522,7 +519,6 @@ nvfp4_status lm_head_sample_ex(const nvfp4_weight* w, const uint16_t* x, int32_t
   if (!aligned(x, 16) || !aligned(max_key, 4) || !aligned(token, 4)) return NVFP4_ERR_ALIGN;
   if (!ws || ws_bytes < lm_head_workspace_bytes(m, w->n)) return NVFP4_ERR_WORKSPACE;
   if (!aligned(ws, 16)) return NVFP4_ERR_ALIGN;
-  if (sm_count() > 1024) return NVFP4_ERR_SHAPE;
   return lm_head_launch(w, x, m, max_key, token, ws, stream, temperature, seed, softcap);
 }
 
@@ -739,13 +735,13 @@ nvfp4_status moe_ffn_grouped(const uint16_t* x, int32_t m, int32_t top_k, const 
 }  // extern "C"
 
 // ------------------------------------------------------------------ lm_head without allocation
-// Scratch for lm_head_argmax_noalloc: the arrival counter (first 4 KiB) and the
-// per-CTA (value, row) partials for up to 1024 CTAs x 16 tokens.  It lives in
-// the library's own device memory, so callers pass only inputs and outputs.
+// Scratch for lm_head_argmax_noalloc: the arrival counter and the per-token
+// packed (value, row) maxima (4 KiB).  It lives in the library's own device
+// memory, so callers pass only inputs and outputs.
 namespace nvfp4 {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = kCounterBytes + static_cast<size_t>(1024) * 16 * (sizeof(float) + sizeof(int));
+constexpr size_t kNoAllocScratchBytes = kCounterBytes;
 static __device__ __align__(256) uint8_t g_lm_head_scratch[kNoAllocScratchBytes];
 
 std::mutex g_scratch_mutex;
@@ -777,7 +773,7 @@ extern "C" nvfp4_status lm_head_argmax_noalloc(const nvfp4_weight* w, const uint
   if (!x || !max_logit || !argmax) return NVFP4_ERR_NULL;
   if (m < 1 || m > 16) return NVFP4_ERR_SHAPE;
   if (!aligned(x, 16) || !aligned(max_logit, 4) || !aligned(argmax, 4)) return NVFP4_ERR_ALIGN;
-  if (lm_head_workspace_bytes(m, w->n) > kNoAllocScratchBytes || sm_count() > 1024) return NVFP4_ERR_WORKSPACE;
+  if (lm_head_workspace_bytes(m, w->n) > kNoAllocScratchBytes) return NVFP4_ERR_WORKSPACE;
   void* ws = nullptr;
   if (const nvfp4_status st = scratch_address(&ws)) return st;
   // the arrival counter must read zero when the kernel starts
