@@ -19,7 +19,7 @@ the 126 MB L2, so no flush is needed between steps.  Step times are the median
 over 20 batches of back-to-back steps (CUDA events at the batch boundaries).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-    python bench.py --profile-case {lm_head,dense4096,dense14336,moe} --m M [--reps R]
+    python bench.py --profile-case {lm_head,dense4096,dense14336,moe,router,step} --m M [--reps R]
 
 Under torchrun (N > 1) every rank runs its own replica (the path needs no
 exchange between GPUs); rank 0 prints one JSON line.  `--impl reference` times
@@ -680,8 +680,11 @@ def profile_case(kind, m, reps):
     """Launch one product `reps` times at one shape: the small single-kernel case a
     profiler capture wants (``ncu -k regex:tc_kernel -s <skip> -c <n> ...``).  Weights
     are seeded N(0, 0.02) fp32 quantized on the GPU, activations N(0, 1) bf16; each
-    repetition launches one kernel (lm_head, dense) or four (moe: route, gate+up,
-    down, combine).  Exits non-zero if the library's device error flag is set."""
+    repetition launches one kernel (lm_head, dense), four (moe: route, gate+up,
+    down, combine) or four (router: the NVFP4 router GEMM with fp32 output, the
+    RMSNorm + scale, the top-k + grouping); `step` runs the whole decode/verify step
+    of the bench (seven launches per repetition, the bench's weights and inputs).
+    Exits non-zero if the library's device error flag is set."""
     import torch
     from nvfp4_w4a16_moe_skinny_gb300 import binding
 
@@ -692,7 +695,16 @@ def profile_case(kind, m, reps):
     def randn(*shape):
         return torch.randn(shape, generator=g, device=dev)
 
-    if kind == "moe":
+    if kind == "step":
+        stream = torch.cuda.Stream(device=dev)
+        wl = build_weights(lib, dev)
+        _, _, _, calls, _ = make_step(lib, wl, m, dev, stream)
+        torch.cuda.synchronize()
+        for _ in range(reps):
+            for _, fn in calls:
+                fn()
+        stream.synchronize()
+    elif kind == "moe":
         e, d, inter = 128, 2816, 704
         gu = lib.prepare(randn(e, 2 * inter, d) * 0.02, gated=True)
         dn = lib.prepare(randn(e, d, inter) * 0.02)
@@ -704,6 +716,15 @@ def profile_case(kind, m, reps):
         for _ in range(reps):
             _, probs, offs, pairs = lib.route_topk(logits, 8)
             lib.moe_ffn(x, 8, probs, offs, pairs, gu, dn, sgu, sdn)
+    elif kind == "router":
+        e, d = 128, 2816
+        wr = lib.prepare(randn(e, d) * 0.02)
+        scale = 1.0 + 0.1 * randn(e)
+        x = randn(m, d).to(torch.bfloat16)
+        torch.cuda.synchronize()
+        for _ in range(reps):
+            logits = lib.router_logits(wr, x, scale)
+            lib.route_topk(logits, 8)
     else:
         shapes = {"lm_head": (262144, 2816), "dense4096": (4096, 4096), "dense14336": (14336, 4096)}
         n, k = shapes[kind]
@@ -732,7 +753,8 @@ def main():
     ap.add_argument("--prefill-m", type=int, default=512,
                     help="also time the MoE layer on a prefill chunk of this many tokens (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=("lm_head", "dense4096", "dense14336", "moe"), default=None)
+    ap.add_argument("--profile-case", choices=("lm_head", "dense4096", "dense14336", "moe", "router", "step"),
+                    default=None)
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:

@@ -152,6 +152,19 @@ nvfp4_status nvfp4_repack(const uint8_t *nibbles, const uint8_t *scales, int32_t
                           int32_t k, uint32_t flags, void *out, cudaStream_t stream);
 
 /*
+ * The same repack on the host: canonical bytes in host memory to the kernel
+ * layout in host memory (the caller copies it to the device).  Byte-identical
+ * to nvfp4_repack() (both walk one index function).  Synchronous; needs no GPU.
+ *   nibbles, scales (host) canonical, as above.
+ *   out      (host) out_bytes >= nvfp4_repacked_bytes(n, k, num_matrices);
+ *            every byte of the repacked size is written (padding with zeros).
+ * Errors: NVFP4_ERR_NULL, NVFP4_ERR_SHAPE, NVFP4_ERR_LAYOUT (unknown flags),
+ * NVFP4_ERR_WORKSPACE (out too small); nothing is written then.
+ */
+nvfp4_status nvfp4_repack_host(const uint8_t *nibbles, const uint8_t *scales, int32_t num_matrices, int32_t n,
+                               int32_t k, uint32_t flags, void *out, size_t out_bytes);
+
+/*
  * Dense skinny GEMM: y[m, :] = bf16( W_hat . x[m, :] ), 1 <= m <= 16.
  *   w   num_matrices == 1, flags == 0.
  *   x   (device) bf16 [m, w->k], 16-byte aligned.

@@ -11,6 +11,7 @@ import ctypes
 import os
 from dataclasses import dataclass
 
+import numpy as np
 import torch
 
 from .build import LIB
@@ -27,6 +28,7 @@ EXPORTS = (
     "nvfp4_gemm", "moe_route_topk", "moe_ffn_workspace_bytes", "moe_ffn_grouped",
     "lm_head_workspace_bytes", "lm_head_argmax", "lm_head_argmax_noalloc", "nvfp4_plan_info",
     "lm_head_sample", "moe_route_topk_ex", "lm_head_sample_ex", "nvfp4_plan_check", "moe_router_logits",
+    "nvfp4_repack_host",
 )
 
 
@@ -104,6 +106,8 @@ def _sig(lib):
     lib.lm_head_sample_ex.restype = ctypes.c_int
     lib.moe_router_logits.argtypes = [ctypes.POINTER(CWeight), _P, _I, _P, ctypes.c_float, _P, _P, _SZ, _P]
     lib.moe_router_logits.restype = ctypes.c_int
+    lib.nvfp4_repack_host.argtypes = [_P, _P, _I, _I, _I, ctypes.c_uint32, _P, _SZ]
+    lib.nvfp4_repack_host.restype = ctypes.c_int
     for name in ("nvfp4_quantize", "nvfp4_repack", "nvfp4_gemm", "moe_route_topk", "moe_ffn_grouped",
                  "lm_head_argmax", "lm_head_argmax_noalloc", "nvfp4_device_error"):
         getattr(lib, name).restype = ctypes.c_int
@@ -182,6 +186,18 @@ class Library:
             nib3.contiguous().data_ptr(), sc3.contiguous().data_ptr(), e, n, k, flags, out.data_ptr(),
             _stream(stream)))
         return Weight(out, gscale.reshape(-1).contiguous().float(), n, k, e, flags)
+
+    def repack_host(self, nib: np.ndarray, sc: np.ndarray, gated: bool = False) -> np.ndarray:
+        """The host-memory repack: canonical u8 [E, n, k/2] / [E, n, k/16] (or 2-D) numpy
+        arrays -> the repacked bytes (u8 numpy)."""
+        nib3 = np.ascontiguousarray(nib.reshape((-1,) + nib.shape[-2:]), np.uint8)
+        sc3 = np.ascontiguousarray(sc.reshape((-1,) + sc.shape[-2:]), np.uint8)
+        e, n, kh = nib3.shape
+        k = 2 * kh
+        out = np.empty((self.repacked_bytes(n, k, e),), dtype=np.uint8)
+        self._check("nvfp4_repack_host", self.lib.nvfp4_repack_host(
+            nib3.ctypes.data, sc3.ctypes.data, e, n, k, NVFP4_GATED if gated else 0, out.ctypes.data, out.nbytes))
+        return out
 
     def prepare(self, w: torch.Tensor, gated: bool = False, stream=None) -> Weight:
         """quantize + repack of fp32 weights already on the GPU."""

@@ -398,6 +398,26 @@ nvfp4_status nvfp4_repack(const uint8_t* nibbles, const uint8_t* scales, int32_t
   return launched();
 }
 
+nvfp4_status nvfp4_repack_host(const uint8_t* nibbles, const uint8_t* scales, int32_t num_matrices, int32_t n,
+                               int32_t k, uint32_t flags, void* out, size_t out_bytes) {
+  if (!nibbles || !scales || !out) return NVFP4_ERR_NULL;
+  if (num_matrices < 1 || n < 1 || k < 16 || (k % 16)) return NVFP4_ERR_SHAPE;
+  if (flags & ~NVFP4_GATED) return NVFP4_ERR_LAYOUT;
+  const bool gated = flags & NVFP4_GATED;
+  if (gated && (n % kGroupRows)) return NVFP4_ERR_SHAPE;
+  if (out_bytes < nvfp4_repacked_bytes(n, k, num_matrices)) return NVFP4_ERR_WORKSPACE;
+  const int ng = ceil_div(n, kGroupRows), kc = ceil_div(k, kTileK);
+  const size_t chunks = static_cast<size_t>(num_matrices) * ng * kc * 4 * 36;
+  uint8_t* dst = static_cast<uint8_t*>(out);
+  for (size_t c = 0; c < chunks; ++c) {
+    uint32_t words[4];
+    repack_chunk(nibbles, scales, n, k, ng, kc, gated, c, words);
+    for (int i = 0; i < 4; ++i)
+      for (int b = 0; b < 4; ++b) dst[16 * c + 4 * i + b] = static_cast<uint8_t>(words[i] >> (8 * b));
+  }
+  return NVFP4_OK;
+}
+
 size_t nvfp4_gemm_workspace_bytes(int32_t m, int32_t n, int32_t k) {
   if (m < 1 || m > 16 || n < 1 || k < 16) return 0;
   return std::max<size_t>(16, fixup_bytes(m, dense_split(m, n, k), ceil_div(n, kGroupRows), 1));

@@ -125,73 +125,78 @@ __global__ void quant_groups_kernel(const float* __restrict__ w, int n, int k, c
   }
 }
 
-// One thread per 16-byte output chunk (36 chunks per 576-byte tile).  Tile t of
-// a matrix is (group G, 64-column chunk kc, 16-row block r) with
+// The 16-byte output chunk c (36 chunks per 576-byte tile) of a repacked stack.
+// Tile t of a matrix is (group G, 64-column chunk kc, 16-row block r) with
 // t = (G * kc_count + kc) * 4 + r (layout version 2: the four tiles of a 64-row
-// group and one chunk are contiguous).
+// group and one chunk are contiguous).  Chunks 0..31 are the A-fragment bytes
+// (lane 4g + t of the m16n8k16 A operand, four 16-column k-steps), 32..35 the
+// tile's 64 scale bytes.  A negative scale is folded into the signs of its 16
+// codes.  The device repack and the host repack both call this.
+__host__ __device__ inline void repack_chunk(const uint8_t* __restrict__ nib, const uint8_t* __restrict__ sc, int n,
+                                             int k, int ng, int kc_count, bool gated, size_t c, uint32_t words[4]) {
+  const int kh = k / 2, kg = k / 16, inter = n / 2;
+  const size_t tiles_per_matrix = static_cast<size_t>(ng) * kc_count * 4;
+  const size_t tile = c / 36;
+  const int part = static_cast<int>(c % 36);
+  const int e = static_cast<int>(tile / tiles_per_matrix);
+  const size_t tm = tile % tiles_per_matrix;
+  const int r = static_cast<int>(tm & 3);
+  const int grp = static_cast<int>((tm >> 2) / kc_count), kc = static_cast<int>((tm >> 2) % kc_count);
+  const int rb = grp * 4 + r;
+  const uint8_t* nib_e = nib + static_cast<size_t>(e) * n * kh;
+  const uint8_t* sc_e = sc + static_cast<size_t>(e) * n * kg;
+  // source row of destination row `dr`, or -1 for padding
+  auto src_row = [&](int dr) -> int {
+    if (gated) {
+      const int blk = dr >> 4, j = dr & 15;
+      return (j < 8) ? (8 * blk + j) : (inter + 8 * blk + (j - 8));
+    }
+    return dr < n ? dr : -1;
+  };
+  if (part < 32) {
+    const int g = part >> 2, t = part & 3;
+    for (int kt = 0; kt < 4; ++kt) {
+      uint32_t wv = 0;
+      for (int rr = 0; rr < 4; ++rr) {
+        const int dr = rb * 16 + g + 8 * (rr & 1);
+        const int col = kc * 64 + kt * 16 + 2 * t + 8 * (rr >> 1);
+        const int sr = src_row(dr);
+        uint32_t byte = 0;
+        if (sr >= 0 && col < k) {
+          byte = nib_e[static_cast<size_t>(sr) * kh + col / 2];
+          if (sc_e[static_cast<size_t>(sr) * kg + col / 16] & 0x80) byte ^= 0x88u;  // fold a negative scale
+        }
+        wv |= byte << (8 * rr);
+      }
+      words[kt] = wv;
+    }
+  } else {
+    // scale bytes 16*(part-32) .. +15 of the 64-byte scale block: byte j -> g = j/8, kt = (j%8)/2, h = j%2
+    for (int wi = 0; wi < 4; ++wi) {
+      uint32_t wv = 0;
+      for (int bi = 0; bi < 4; ++bi) {
+        const int j = 16 * (part - 32) + 4 * wi + bi;
+        const int g = j >> 3, kt = (j & 7) >> 1, h = j & 1;
+        const int dr = rb * 16 + g + 8 * h;
+        const int grp16 = kc * 4 + kt;
+        const int sr = src_row(dr);
+        uint32_t byte = 0;
+        if (sr >= 0 && grp16 < kg) byte = sc_e[static_cast<size_t>(sr) * kg + grp16] & 0x7Fu;
+        wv |= byte << (8 * bi);
+      }
+      words[wi] = wv;
+    }
+  }
+}
+
+// One thread per 16-byte output chunk.
 __global__ void repack_kernel(const uint8_t* __restrict__ nib, const uint8_t* __restrict__ sc, int n, int k, int ng,
                               int kc_count, bool gated, size_t tiles_total, uint8_t* __restrict__ out) {
   const size_t chunks = tiles_total * 36;
-  const int kh = k / 2, kg = k / 16, inter = n / 2;
-  const size_t tiles_per_matrix = static_cast<size_t>(ng) * kc_count * 4;
   for (size_t c = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks;
        c += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t tile = c / 36;
-    const int part = static_cast<int>(c % 36);
-    const int e = static_cast<int>(tile / tiles_per_matrix);
-    const size_t tm = tile % tiles_per_matrix;
-    const int r = static_cast<int>(tm & 3);
-    const int grp = static_cast<int>((tm >> 2) / kc_count), kc = static_cast<int>((tm >> 2) % kc_count);
-    const int rb = grp * 4 + r;
-    const uint8_t* nib_e = nib + static_cast<size_t>(e) * n * kh;
-    const uint8_t* sc_e = sc + static_cast<size_t>(e) * n * kg;
-    // source row of destination row `dr`, or -1 for padding
-    auto src_row = [&](int dr) -> int {
-      if (gated) {
-        const int blk = dr >> 4, j = dr & 15;
-        return (j < 8) ? (8 * blk + j) : (inter + 8 * blk + (j - 8));
-      }
-      return dr < n ? dr : -1;
-    };
     uint32_t words[4];
-    if (part < 32) {
-      const int g = part >> 2, t = part & 3;
-#pragma unroll
-      for (int kt = 0; kt < 4; ++kt) {
-        uint32_t wv = 0;
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-          const int dr = rb * 16 + g + 8 * (rr & 1);
-          const int col = kc * 64 + kt * 16 + 2 * t + 8 * (rr >> 1);
-          const int sr = src_row(dr);
-          uint32_t byte = 0;
-          if (sr >= 0 && col < k) {
-            byte = nib_e[static_cast<size_t>(sr) * kh + col / 2];
-            if (sc_e[static_cast<size_t>(sr) * kg + col / 16] & 0x80) byte ^= 0x88u;  // fold a negative scale
-          }
-          wv |= byte << (8 * rr);
-        }
-        words[kt] = wv;
-      }
-    } else {
-      // scale bytes 16*(part-32) .. +15 of the 64-byte scale block: byte j -> g = j/8, kt = (j%8)/2, h = j%2
-#pragma unroll
-      for (int wi = 0; wi < 4; ++wi) {
-        uint32_t wv = 0;
-#pragma unroll
-        for (int bi = 0; bi < 4; ++bi) {
-          const int j = 16 * (part - 32) + 4 * wi + bi;
-          const int g = j >> 3, kt = (j & 7) >> 1, h = j & 1;
-          const int dr = rb * 16 + g + 8 * h;
-          const int grp16 = kc * 4 + kt;
-          const int sr = src_row(dr);
-          uint32_t byte = 0;
-          if (sr >= 0 && grp16 < kg) byte = sc_e[static_cast<size_t>(sr) * kg + grp16] & 0x7Fu;
-          wv |= byte << (8 * bi);
-        }
-        words[wi] = wv;
-      }
-    }
+    repack_chunk(nib, sc, n, k, ng, kc_count, gated, c, words);
     reinterpret_cast<uint4*>(out)[c] = make_uint4(words[0], words[1], words[2], words[3]);
   }
 }

@@ -6,6 +6,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 from nvfp4_w4a16_moe_skinny_gb300 import build as B
@@ -147,3 +148,49 @@ def test_binding_refuses_to_run_without_the_library(tmp_path):
     from nvfp4_w4a16_moe_skinny_gb300 import binding
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         binding.Library(str(tmp_path / "missing.so"))
+
+
+def _host_repack(so, nib, sc, gated):
+    e, n, kh = nib.shape
+    k = 2 * kh
+    out = (ctypes.c_uint8 * OL.repacked_bytes(n, k, e))()
+    nib = np.ascontiguousarray(nib)
+    sc = np.ascontiguousarray(sc)
+    st = so.nvfp4_repack_host(nib.ctypes.data, sc.ctypes.data, e, n, k, 1 if gated else 0, out, len(out))
+    assert st == 0
+    return np.frombuffer(out, dtype=np.uint8)
+
+
+@pytest.mark.parametrize("e,n,k,gated", [(1, 16, 64, False), (2, 40, 80, False), (1, 1000, 320, False),
+                                         (3, 64, 128, True), (2, 128, 16, True), (1, 192, 704, True)])
+def test_host_repack_matches_the_layout_definition(so, e, n, k, gated):
+    """The host repack (host bytes in, host bytes out) against the oracle's index
+    function of the layout, byte for byte, including the zero padding."""
+    rng = np.random.default_rng(n * 5 + k)
+    nib = rng.integers(0, 256, (e, n, k // 2), dtype=np.uint8)
+    sc = rng.integers(0, 127, (e, n, k // 16), dtype=np.uint8)
+    assert np.array_equal(_host_repack(so, nib, sc, gated), OL.repack(nib, sc, gated))
+
+
+def test_host_repack_folds_negative_scales(so):
+    """A scale byte with bit 7 set is stored positive and its 16 codes change sign:
+    the dequantized matrix is unchanged."""
+    from oracle import formats as F
+    rng = np.random.default_rng(6)
+    n, k = 48, 128
+    nib = rng.integers(0, 256, (1, n, k // 2), dtype=np.uint8)
+    sc = rng.integers(1, 127, (1, n, k // 16), dtype=np.uint8)
+    sc[0, ::3, 1] |= 0x80
+    nib2, sc2 = OL.unrepack(_host_repack(so, nib, sc, False), n, k)
+    assert not (sc2 & 0x80).any()
+    assert np.array_equal(F.dequantize_matrix(nib2[0], sc2[0], 1.0), F.dequantize_matrix(nib[0], sc[0], 1.0))
+
+
+def test_host_repack_rejects_bad_arguments(so):
+    buf = (ctypes.c_uint8 * 64)()
+    small = (ctypes.c_uint8 * 16)()
+    assert so.nvfp4_repack_host(None, buf, 1, 16, 64, 0, buf, 64) == 1                    # null
+    assert so.nvfp4_repack_host(buf, buf, 1, 16, 60, 0, buf, 64) != 0                     # k % 16
+    assert so.nvfp4_repack_host(buf, buf, 1, 40, 64, 1, buf, 64) != 0                     # gated n % 64
+    assert so.nvfp4_repack_host(buf, buf, 1, 16, 64, 4, buf, 64) != 0                     # unknown flag
+    assert so.nvfp4_repack_host(buf, buf, 1, 16, 64, 0, small, 16) != 0                   # out too small

@@ -92,6 +92,18 @@ def test_repack_bytes_bit_exact(lib, e, n, k, gated):
     assert np.array_equal(wt.data.cpu().numpy(), OL.repack(nib, sc, gated))
 
 
+def test_device_and_host_repack_agree(lib):
+    """The device repack and the host repack give the same bytes on a stacked gated
+    weight with negative scales."""
+    rng = np.random.default_rng(17)
+    e, n, k = 3, 256, 704
+    nib = rng.integers(0, 256, (e, n, k // 2), dtype=np.uint8)
+    sc = rng.integers(0, 256, (e, n, k // 16), dtype=np.uint8)
+    wt = lib.repack(torch.from_numpy(nib).to(dev()), torch.from_numpy(sc).to(dev()), torch.ones(e, device=dev()),
+                    gated=True)
+    assert np.array_equal(wt.data.cpu().numpy(), lib.repack_host(nib, sc, gated=True))
+
+
 def test_repack_folds_negative_scales(lib):
     rng = np.random.default_rng(5)
     n, k = 32, 64
@@ -136,6 +148,50 @@ def test_tiny_gemm_config0(lib):
 def test_gemm_ragged_all_m(lib, m, n, k):
     got, exact, absy = _dense(lib, m, n, k, 1000 + n + k, 2000 + m)
     check_bound(got, exact, absy, True, f"gemm m={m} n={n} k={k}")
+
+
+def _wide_range_case(m, n, k, small_exp, big_cols_weight):
+    """x rows with 2^10 at every 64th column and +-2^small_exp * (1 + j/256) elsewhere;
+    the weight's columns under the large values are zero unless big_cols_weight."""
+    rng = np.random.default_rng(77)
+    w = W.weight((n, k), 4242)
+    big = np.arange(k) % 64 == 0
+    if not big_cols_weight:
+        w[:, big] = 0.0
+    frac = rng.integers(0, 256, size=(m, k)) / 256.0
+    sign = np.where(rng.random((m, k)) < 0.5, -1.0, 1.0)
+    x = (sign * (1.0 + frac) * 2.0 ** small_exp).astype(np.float32)
+    x[:, big] = 2.0 ** 10
+    xb = W.to_bf16_bits(x)
+    assert np.array_equal(W.bf16_bits_to_f32(xb), x)      # every value is a bf16
+    nib, sc, g = F.quantize_matrix(w)
+    return (nib, sc, g), xb, x
+
+
+@pytest.mark.parametrize("m", [1, 5, 8, 16])
+def test_gemm_activation_dynamic_range(lib, m):
+    """The tensor-core and CUDA-core paths take the bf16 activations as f16 after a
+    per-row power-of-two rescale that puts the row maximum (over the staged columns)
+    in [2^14, 2^15).  A bf16 value 2^31 or less below the maximum keeps every bit; one
+    more than 2^38 below it falls under f16's smallest subnormal and is dropped.
+    (a) Small values 2^30 below the large ones, the weights under the large values
+    zero, so the result is made of the small values alone: within the bound.
+    (b) The same rows with the small values 2^50 below: they are dropped, and the
+    result is exactly zero (the documented limit of the f16 operands).
+    (c) 2^50 of range with the large values weighted: within the bound, since the
+    dropped terms are below 2^-38 of the largest term."""
+    n, k = 192, 1024
+    for small_exp, weighted, what in ((-20, False, "a"), (-40, False, "b"), (-40, True, "c")):
+        q, xb, x = _wide_range_case(m, n, k, small_exp, weighted)
+        wt = upload_oracle_weight(lib, q)
+        y = bf16_to_f64(lib.gemm(wt, upload_bf16(xb)))
+        torch.cuda.synchronize()
+        exact, _, absy = OG.nvfp4_gemm(*q, x.astype(np.float64))
+        if what == "b":
+            assert np.all(y == 0.0) and np.all(exact != 0.0), "values 2^50 below the row maximum were not dropped"
+        else:
+            check_bound(y, exact, absy, True, f"dynamic range case {what} m={m}")
+    assert lib.device_error() == 0
 
 
 _DENSE_FULL = {}
