@@ -376,7 +376,9 @@ nvfp4_status nvfp4_plan_info(int32_t product, int32_t m, int32_t n, int32_t k, i
  *        K-split counter in its fixed area (else 0); the largest staged column
  *        span; the planned span capacity; the most segments one CTA stages; the
  *        planned segment capacity; the tiles and the pieces walked; the dynamic
- *        shared memory bytes.
+ *        shared memory bytes; and, if out_len >= 10, the most (16-row tile x
+ *        64-column chunk) steps any warp of the decode kernel streams and the
+ *        mean over all warps, rounded up (both 0 for the prefill kernel).
  * Returns NVFP4_ERR_SHAPE for rejected shapes or n_seg above the plan's capacity.
  */
 nvfp4_status nvfp4_plan_check(int32_t product, int32_t m, int32_t n, int32_t k, int32_t top_k, int32_t n_experts,

@@ -854,6 +854,7 @@ extern "C" nvfp4_status nvfp4_plan_check(int32_t product, int32_t m, int32_t n, 
   Plan pl;
   if (!product_plan(product, m, n, k, top_k, n_experts, sms, &pl)) return NVFP4_ERR_SHAPE;
   if (n_seg > pl.max_segs) return NVFP4_ERR_SHAPE;
+  long long warp_max = 0, warp_sum = 0;  // (tile x chunk) steps per warp, decode kernel
   const int ng = ceil_div(n, kGroupRows), kc = ceil_div(k, kTileK);
   const long long cells = static_cast<long long>(n_seg) * ng * 4 * pl.S;  // (segment, group, tile, slice)
   if (cells > (1ll << 27)) return NVFP4_ERR_SHAPE;
@@ -881,13 +882,18 @@ extern "C" nvfp4_status nvfp4_plan_check(int32_t product, int32_t m, int32_t n, 
       dd.span(u0, u1, cseg0, nsc, c_lo, c_hi);
       max_span = std::max(max_span, c_hi - c_lo);
       max_segs = std::max(max_segs, nsc);
-      for (int w = 0; w < kWarps; ++w)
+      for (int w = 0; w < kWarps; ++w) {
+        long long work = 0;
         for (int j = 0; j < dd.n_pieces(u1 - u0, w); ++j) {
           const Piece pc = dd.piece(u0, u1 - u0, w, j);
           const int c0 = pc.s * pl.L, c1 = c0 + dd.slice_len(pc.s);
           if (c0 < c_lo || c1 > c_hi || pc.seg < cseg0 || pc.seg >= cseg0 + nsc) ++bad;  // inside the staged span
           take(pc);
+          work += static_cast<long long>(pc.tn) * (c1 - c0);
         }
+        warp_max = std::max(warp_max, work);
+        warp_sum += work;
+      }
     }
   } else {
     const PrefillDeal pd{n_seg, pl.S, pl.L, kc, ng, pl.grid};
@@ -917,5 +923,10 @@ extern "C" nvfp4_status nvfp4_plan_check(int32_t product, int32_t m, int32_t n, 
   out[5] = static_cast<int32_t>(std::min<long long>(tiles, 0x7FFFFFFF));
   out[6] = static_cast<int32_t>(std::min<long long>(pieces, 0x7FFFFFFF));
   out[7] = static_cast<int32_t>(pl.smem);
+  if (out_len >= 10) {  // the busiest warp's (tile x chunk) steps and the mean over all warps, rounded up
+    const long long warps = static_cast<long long>(pl.grid) * kWarps;
+    out[8] = static_cast<int32_t>(std::min<long long>(warp_max, 0x7FFFFFFF));
+    out[9] = static_cast<int32_t>(std::min<long long>((warp_sum + warps - 1) / warps, 0x7FFFFFFF));
+  }
   return NVFP4_OK;
 }

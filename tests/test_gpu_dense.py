@@ -151,14 +151,14 @@ def test_gemm_ragged_all_m(lib, m, n, k):
 
 
 def _wide_range_case(m, n, k, small_exp, big_cols_weight):
-    """x rows with 2^10 at every 64th column and +-2^small_exp * (1 + j/256) elsewhere;
+    """x rows with 2^10 at every 64th column and +-2^small_exp * (1 + j/128) elsewhere;
     the weight's columns under the large values are zero unless big_cols_weight."""
     rng = np.random.default_rng(77)
     w = W.weight((n, k), 4242)
     big = np.arange(k) % 64 == 0
     if not big_cols_weight:
         w[:, big] = 0.0
-    frac = rng.integers(0, 256, size=(m, k)) / 256.0
+    frac = rng.integers(0, 128, size=(m, k)) / 128.0
     sign = np.where(rng.random((m, k)) < 0.5, -1.0, 1.0)
     x = (sign * (1.0 + frac) * 2.0 ** small_exp).astype(np.float32)
     x[:, big] = 2.0 ** 10

@@ -119,6 +119,16 @@ def test_lm_head_plan_covers_every_tile_once(so, m):
     assert pl["S"] == 1  # the lm_head never splits K
 
 
+def test_busiest_warp_report(so):
+    """The walk reports the busiest warp's (tile x chunk) steps against the mean: the
+    lm_head's 26-27 whole 64-row groups per CTA over 16 warps give warps one or two
+    groups (2 x 4 tiles x 44 chunks = 352 against a mean of ~297)."""
+    out = (ctypes.c_int32 * 10)()
+    assert so.nvfp4_plan_check(1, 15, 262144, 2816, 0, 0, 152, 1, out, 10) == 0
+    assert out[0] == 1 and out[8] == 2 * 4 * 44
+    assert out[9] == -(-262144 // 64 * 4 * 44 // (152 * 16))
+
+
 @pytest.mark.parametrize("m,top_k,n_exp,d,inter", [
     (1, 8, 128, 2816, 704), (15, 8, 128, 2816, 704), (16, 8, 128, 2816, 704), (512, 8, 128, 2816, 704),
     (2, 3, 8, 128, 64), (16, 2, 6, 192, 128), (40, 3, 8, 128, 64), (100, 1, 40, 192, 128), (17, 2, 6, 192, 128)])
