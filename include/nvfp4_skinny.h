@@ -183,6 +183,38 @@ nvfp4_status nvfp4_gemm(const nvfp4_weight *w, const uint16_t *x, int32_t m, uin
                         size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * W4A4 NVFP4 (activations quantized too).  The pages do not describe this
+ * variant; it follows the weights' recipe (gemma-cuda-hybrid README,
+ * "Everything it has / Inference engine": E2M1 codes, E4M3 scales per 16
+ * along K, an FP32 global scale), with one global scale per token row.
+ *
+ * nvfp4_quantize_act: bf16 activations -> NVFP4, each row quantized as a matrix
+ * of its own (the codes and scales decided as in nvfp4_quantize), so a token's
+ * codes do not depend on the rest of the batch.
+ *   x             (device) bf16 [m, k], 1 <= m <= 4096, k % 16 == 0, 16-byte aligned.
+ *   codes         (device) u8 [m, k/2] canonical (column 2i in the low nibble of
+ *                 byte i), 8-byte aligned;  scales (device) u8 [m, k/16].
+ *   global_scale  (device) fp32 [m]: amax of row m / 2688.
+ *   ws            (device) nvfp4_quantize_workspace_bytes(m) bytes.
+ *
+ * nvfp4_gemm_w4a4 / lm_head_argmax_w4a4: nvfp4_gemm and lm_head_argmax with
+ * the activations given as the output of nvfp4_quantize_act:
+ *   y[m, n] = bf16( sum_k w_hat[n, k] * x_hat[m, k] ),
+ *   x_hat[m, k] = e2m1(code) * e4m3(scale of k's 16-group) * global_scale[m].
+ * x_codes 16-byte aligned, k = w->k.  The activations are dequantized into f16
+ * tensor-core operands (exact) as the weights are; fp32 accumulation.
+ * Workspaces and limits as nvfp4_gemm / lm_head_argmax (1 <= m <= 16).
+ */
+nvfp4_status nvfp4_quantize_act(const uint16_t *x, int32_t m, int32_t k, uint8_t *codes, uint8_t *scales,
+                                float *global_scale, void *ws, size_t ws_bytes, cudaStream_t stream);
+nvfp4_status nvfp4_gemm_w4a4(const nvfp4_weight *w, const uint8_t *x_codes, const uint8_t *x_scales,
+                             const float *x_global, int32_t m, uint16_t *y, void *ws, size_t ws_bytes,
+                             cudaStream_t stream);
+nvfp4_status lm_head_argmax_w4a4(const nvfp4_weight *w, const uint8_t *x_codes, const uint8_t *x_scales,
+                                 const float *x_global, int32_t m, float *max_logit, int32_t *argmax, void *ws,
+                                 size_t ws_bytes, cudaStream_t stream);
+
+/*
  * Router logits from the hidden state (TensorSharp docs/models/gemma4.md, "4.6
  * MoE", step 2: the router matmul, an unweighted RMSNorm, then the learned
  * per-expert scale ffn_gate_inp.scale):

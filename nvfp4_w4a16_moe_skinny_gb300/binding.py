@@ -28,7 +28,7 @@ EXPORTS = (
     "nvfp4_gemm", "moe_route_topk", "moe_ffn_workspace_bytes", "moe_ffn_grouped",
     "lm_head_workspace_bytes", "lm_head_argmax", "lm_head_argmax_noalloc", "nvfp4_plan_info",
     "lm_head_sample", "moe_route_topk_ex", "lm_head_sample_ex", "nvfp4_plan_check", "moe_router_logits",
-    "nvfp4_repack_host",
+    "nvfp4_repack_host", "nvfp4_quantize_act", "nvfp4_gemm_w4a4", "lm_head_argmax_w4a4",
 )
 
 
@@ -106,6 +106,12 @@ def _sig(lib):
     lib.lm_head_sample_ex.restype = ctypes.c_int
     lib.moe_router_logits.argtypes = [ctypes.POINTER(CWeight), _P, _I, _P, ctypes.c_float, _P, _P, _SZ, _P]
     lib.moe_router_logits.restype = ctypes.c_int
+    lib.nvfp4_quantize_act.argtypes = [_P, _I, _I, _P, _P, _P, _P, _SZ, _P]
+    lib.nvfp4_quantize_act.restype = ctypes.c_int
+    lib.nvfp4_gemm_w4a4.argtypes = [ctypes.POINTER(CWeight), _P, _P, _P, _I, _P, _P, _SZ, _P]
+    lib.nvfp4_gemm_w4a4.restype = ctypes.c_int
+    lib.lm_head_argmax_w4a4.argtypes = [ctypes.POINTER(CWeight), _P, _P, _P, _I, _P, _P, _P, _SZ, _P]
+    lib.lm_head_argmax_w4a4.restype = ctypes.c_int
     lib.nvfp4_repack_host.argtypes = [_P, _P, _I, _I, _I, ctypes.c_uint32, _P, _SZ]
     lib.nvfp4_repack_host.restype = ctypes.c_int
     for name in ("nvfp4_quantize", "nvfp4_repack", "nvfp4_gemm", "moe_route_topk", "moe_ffn_grouped",
@@ -227,6 +233,46 @@ class Library:
         self._check("lm_head_argmax", self.lib.lm_head_argmax(
             ctypes.byref(cw), x.data_ptr(), m, out[0].data_ptr(), out[1].data_ptr(), ws.data_ptr(), ws.numel(),
             _stream(stream)))
+        return out
+
+    # -------------------------------------------------------------- W4A4
+    def quantize_act(self, x: torch.Tensor, out=None, stream=None):
+        """bf16 activations [m, k] -> NVFP4 per token row: (codes u8 [m, k/2], scales u8
+        [m, k/16], global scales fp32 [m])."""
+        m, k = x.shape
+        if out is None:
+            out = (torch.empty((m, k // 2), dtype=torch.uint8, device=x.device),
+                   torch.empty((m, k // 16), dtype=torch.uint8, device=x.device),
+                   torch.empty((m,), dtype=torch.float32, device=x.device))
+        ws = self.workspace("quantize_act", max(16, self.lib.nvfp4_quantize_workspace_bytes(m)), x.device)
+        self._check("nvfp4_quantize_act", self.lib.nvfp4_quantize_act(
+            x.data_ptr(), m, k, out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(), ws.data_ptr(), ws.numel(),
+            _stream(stream)))
+        return out
+
+    def gemm_w4a4(self, w: Weight, xq, y: torch.Tensor = None, stream=None) -> torch.Tensor:
+        codes, scales, g = xq
+        m = codes.shape[0]
+        if y is None:
+            y = torch.empty((m, w.n), dtype=torch.bfloat16, device=codes.device)
+        ws = self.workspace("gemm", self.lib.nvfp4_gemm_workspace_bytes(m, w.n, w.k), codes.device)
+        cw = w.c()
+        self._check("nvfp4_gemm_w4a4", self.lib.nvfp4_gemm_w4a4(
+            ctypes.byref(cw), codes.data_ptr(), scales.data_ptr(), g.data_ptr(), m, y.data_ptr(), ws.data_ptr(),
+            ws.numel(), _stream(stream)))
+        return y
+
+    def lm_head_argmax_w4a4(self, w: Weight, xq, out=None, stream=None):
+        codes, scales, g = xq
+        m = codes.shape[0]
+        if out is None:
+            out = (torch.empty((m,), dtype=torch.float32, device=codes.device),
+                   torch.empty((m,), dtype=torch.int32, device=codes.device))
+        ws = self.workspace("lm_head", self.lib.lm_head_workspace_bytes(m, w.n), codes.device)
+        cw = w.c()
+        self._check("lm_head_argmax_w4a4", self.lib.lm_head_argmax_w4a4(
+            ctypes.byref(cw), codes.data_ptr(), scales.data_ptr(), g.data_ptr(), m, out[0].data_ptr(),
+            out[1].data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
         return out
 
     def lm_head_sample(self, w: Weight, x: torch.Tensor, temperature: float, seed: int, out=None, stream=None,

@@ -93,6 +93,9 @@ struct Job {
   float inv_temp;         // kEpiSample: 1 / temperature
   uint32_t seed_lo, seed_hi;  // kEpiSample: the Philox key of this call's noise
   float softcap;          // kEpiArgmax / kEpiSample: cap of cap * tanh(logit / cap) (0: off)
+  const uint8_t* xq;      // W4A4 (dense jobs): NVFP4 activation codes [m, k/2] instead of x ...
+  const uint8_t* xq_sc;   //   ... their E4M3 scales [m, k/16]
+  const float* xq_g;      //   ... and per-row global scales [m]
 };
 
 __host__ __device__ inline size_t stream_table_bytes(int n_experts) {
@@ -416,12 +419,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (early) pdl_wait();
   pdl_launch_dependents();
 
-  stage_rows<kMMA>(p.x, p.k, c_lo * kTileK, c_hi - c_lo, nrows, row_src, sigma, xs, stride, issue_rest);
+  if (p.xq)  // W4A4: the rows are NVFP4 already
+    stage_rows_fp4<kMMA>(p.xq, p.xq_sc, p.k, c_lo * kTileK, c_hi - c_lo, nrows, row_src, sigma, xs, stride,
+                         issue_rest);
+  else
+    stage_rows<kMMA>(p.x, p.k, c_lo * kTileK, c_hi - c_lo, nrows, row_src, sigma, xs, stride, issue_rest);
   if (threadIdx.x < nsc_used * 16) {
     const int e = seg_list[cseg0 + (threadIdx.x >> 4)];
     const float gsc = (e == kSharedSeg) ? __ldg(p.gs_sh) : (e == kDenseSeg ? __ldg(p.gs) : __ldg(p.gs + e));
     const int row = slot_row[threadIdx.x];
-    mul[threadIdx.x] = row < nrows ? gsc * exp2i(8 - sigma[row]) : 0.f;
+    // (W4A4, dense jobs: staged row j is token j, with its own global scale)
+    mul[threadIdx.x] = row < nrows ? gsc * exp2i(8 - sigma[row]) * (p.xq_g ? __ldg(p.xq_g + row) : 1.f) : 0.f;
   }
   __syncthreads();
 

@@ -363,8 +363,16 @@ size_t nvfp4_quantize_workspace_bytes(int32_t num_matrices) {
   return num_matrices < 1 ? 0 : static_cast<size_t>(num_matrices) * sizeof(unsigned);
 }
 
-nvfp4_status nvfp4_quantize(const float* w, int32_t num_matrices, int32_t n, int32_t k, uint8_t* nibbles,
-                            uint8_t* scales, float* global_scale, void* ws, size_t ws_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace nvfp4 {
+namespace {
+
+// The quantizer's two grids over num_matrices matrices of [n, k] elements of T
+// (fp32 weights or bf16 activation rows): per-matrix amax, then the codes.
+template <typename T>
+nvfp4_status quantize_launch(const T* w, int32_t num_matrices, int32_t n, int32_t k, uint8_t* nibbles,
+                             uint8_t* scales, float* global_scale, void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (!w || !nibbles || !scales || !global_scale) return NVFP4_ERR_NULL;
   if (num_matrices < 1 || n < 1 || k < 16 || (k % 16)) return NVFP4_ERR_SHAPE;
   if (!ws || ws_bytes < nvfp4_quantize_workspace_bytes(num_matrices)) return NVFP4_ERR_WORKSPACE;
@@ -374,12 +382,29 @@ nvfp4_status nvfp4_quantize(const float* w, int32_t num_matrices, int32_t n, int
   const size_t per = static_cast<size_t>(n) * k;
   const int sms = std::max(1, sm_count());
   const int bx = static_cast<int>(std::min<size_t>((per + 255) / 256, static_cast<size_t>(sms) * 4));
-  quant_amax_kernel<<<dim3(bx, num_matrices), 256, 0, stream>>>(w, per, amax);
+  quant_amax_kernel<T><<<dim3(bx, num_matrices), 256, 0, stream>>>(w, per, amax);
   if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   const size_t groups = per / 16;
   const int gx = static_cast<int>(std::min<size_t>((groups + 255) / 256, static_cast<size_t>(sms) * 8));
-  quant_groups_kernel<<<dim3(gx, num_matrices), 256, 0, stream>>>(w, n, k, amax, nibbles, scales, global_scale);
+  quant_groups_kernel<T><<<dim3(gx, num_matrices), 256, 0, stream>>>(w, n, k, amax, nibbles, scales, global_scale);
   return launched();
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" {
+
+nvfp4_status nvfp4_quantize(const float* w, int32_t num_matrices, int32_t n, int32_t k, uint8_t* nibbles,
+                            uint8_t* scales, float* global_scale, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return quantize_launch(w, num_matrices, n, k, nibbles, scales, global_scale, ws, ws_bytes, stream);
+}
+
+nvfp4_status nvfp4_quantize_act(const uint16_t* x, int32_t m, int32_t k, uint8_t* codes, uint8_t* scales,
+                                float* global_scale, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (m > 4096) return NVFP4_ERR_SHAPE;
+  // each token row is a matrix of its own: one global scale per row
+  return quantize_launch(x, m, 1, k, codes, scales, global_scale, ws, ws_bytes, stream);
 }
 
 nvfp4_status nvfp4_repack(const uint8_t* nibbles, const uint8_t* scales, int32_t num_matrices, int32_t n, int32_t k,
@@ -443,6 +468,28 @@ nvfp4_status nvfp4_gemm(const nvfp4_weight* w, const uint16_t* x, int32_t m, uin
   return dispatch_stream<kEpiStore>(p, maps, plan, stream);
 }
 
+nvfp4_status nvfp4_gemm_w4a4(const nvfp4_weight* w, const uint8_t* x_codes, const uint8_t* x_scales,
+                             const float* x_global, int32_t m, uint16_t* y, void* ws, size_t ws_bytes,
+                             cudaStream_t stream) {
+  if (const nvfp4_status st = check_weight(w, 1, 0)) return st;
+  if (!x_codes || !x_scales || !x_global || !y) return NVFP4_ERR_NULL;
+  if (m < 1 || m > 16) return NVFP4_ERR_SHAPE;
+  if (!aligned(x_codes, 16) || !aligned(x_global, 4) || !aligned(y, 4)) return NVFP4_ERR_ALIGN;
+  if (!ws || ws_bytes < nvfp4_gemm_workspace_bytes(m, w->n, w->k)) return NVFP4_ERR_WORKSPACE;
+  if (!aligned(ws, 16)) return NVFP4_ERR_ALIGN;
+  Job p = dense_job(w, nullptr, m);
+  p.xq = x_codes, p.xq_sc = x_scales, p.xq_g = x_global;
+  p.y = y;
+  p.y_ld = w->n;
+  set_fixup(&p, ws);
+  Plan plan;
+  if (!make_plan(m, dense_split(m, w->n, w->k), p.ng, p.kc, 1, 0, false, false, std::max(1, sm_count()), &plan))
+    return NVFP4_ERR_SHAPE;
+  WeightMaps maps;
+  if (!make_maps(w, nullptr, &maps)) return NVFP4_ERR_CUDA;
+  return dispatch_stream<kEpiStore>(p, maps, plan, stream);
+}
+
 nvfp4_status moe_router_logits(const nvfp4_weight* w, const uint16_t* x, int32_t m, const float* gate_scale, float eps,
                                float* logits, void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (const nvfp4_status st = check_weight(w, 1, 0)) return st;
@@ -483,8 +530,10 @@ namespace {
 // The lm_head grid: greedy argmax, or (temperature > 0) the Gumbel-max sample.
 nvfp4_status lm_head_launch(const nvfp4_weight* w, const uint16_t* x, int32_t m, float* max_logit, int32_t* argmax,
                             void* ws, cudaStream_t stream, float temperature = 0.f, uint64_t seed = 0,
-                            float softcap = 0.f) {
+                            float softcap = 0.f, const uint8_t* xq = nullptr, const uint8_t* xq_sc = nullptr,
+                            const float* xq_g = nullptr) {
   Job p = dense_job(w, x, m);
+  p.xq = xq, p.xq_sc = xq_sc, p.xq_g = xq_g;
   p.softcap = softcap;
   p.am_cnt = static_cast<unsigned*>(ws);
   p.am_key = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + 64);
@@ -516,6 +565,19 @@ nvfp4_status lm_head_argmax(const nvfp4_weight* w, const uint16_t* x, int32_t m,
   if (!ws || ws_bytes < lm_head_workspace_bytes(m, w->n)) return NVFP4_ERR_WORKSPACE;
   if (!aligned(ws, 16)) return NVFP4_ERR_ALIGN;
   return lm_head_launch(w, x, m, max_logit, argmax, ws, stream);
+}
+
+nvfp4_status lm_head_argmax_w4a4(const nvfp4_weight* w, const uint8_t* x_codes, const uint8_t* x_scales,
+                                 const float* x_global, int32_t m, float* max_logit, int32_t* argmax, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
+  if (const nvfp4_status st = check_weight(w, 1, 0)) return st;
+  if (!x_codes || !x_scales || !x_global || !max_logit || !argmax) return NVFP4_ERR_NULL;
+  if (m < 1 || m > 16) return NVFP4_ERR_SHAPE;
+  if (!aligned(x_codes, 16) || !aligned(x_global, 4) || !aligned(max_logit, 4) || !aligned(argmax, 4))
+    return NVFP4_ERR_ALIGN;
+  if (!ws || ws_bytes < lm_head_workspace_bytes(m, w->n)) return NVFP4_ERR_WORKSPACE;
+  if (!aligned(ws, 16)) return NVFP4_ERR_ALIGN;
+  return lm_head_launch(w, nullptr, m, max_logit, argmax, ws, stream, 0.f, 0, 0.f, x_codes, x_scales, x_global);
 }
 
 nvfp4_status lm_head_sample(const nvfp4_weight* w, const uint16_t* x, int32_t m, float temperature, uint64_t seed,

@@ -20,16 +20,45 @@
 
 namespace nvfp4 {
 
+// An input element as fp32: fp32 weights, or bf16 activations (exact).
+__device__ __forceinline__ float in_value(float v) { return v; }
+__device__ __forceinline__ float in_value(uint16_t v) { return __uint_as_float(static_cast<uint32_t>(v) << 16); }
+
+// 16 consecutive input elements (16-element aligned) as fp32.
+__device__ __forceinline__ void load16(const float* __restrict__ p, float (&v)[16]) {
+  const float4* src = reinterpret_cast<const float4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = src[i];
+    v[4 * i] = f.x, v[4 * i + 1] = f.y, v[4 * i + 2] = f.z, v[4 * i + 3] = f.w;
+  }
+}
+__device__ __forceinline__ void load16(const uint16_t* __restrict__ p, float (&v)[16]) {
+  const uint4* src = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint4 u = src[i];
+    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * i + 2 * j] = __uint_as_float(w4[j] << 16);
+      v[8 * i + 2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+    }
+  }
+}
+
 // Per-matrix amax of |w| as the bit pattern of a non-negative float: for such
 // floats unsigned integer order equals numeric order, so atomicMax is exact and
-// order-independent.
-__global__ void quant_amax_kernel(const float* __restrict__ w, size_t per_matrix, unsigned* __restrict__ amax_bits) {
+// order-independent.  T: float (weights) or uint16_t (bf16 activations, one
+// "matrix" per token row).
+template <typename T>
+__global__ void quant_amax_kernel(const T* __restrict__ w, size_t per_matrix, unsigned* __restrict__ amax_bits) {
   const int e = blockIdx.y;
-  const float* src = w + static_cast<size_t>(e) * per_matrix;
+  const T* src = w + static_cast<size_t>(e) * per_matrix;
   unsigned best = 0;
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < per_matrix;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const unsigned b = __float_as_uint(fabsf(src[i]));
+    const unsigned b = __float_as_uint(fabsf(in_value(src[i])));
     best = b > best ? b : best;
   }
   for (int off = 16; off > 0; off >>= 1) {
@@ -81,7 +110,8 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
 }
 
 // One thread per 16-element group.
-__global__ void quant_groups_kernel(const float* __restrict__ w, int n, int k, const unsigned* __restrict__ amax_bits,
+template <typename T>
+__global__ void quant_groups_kernel(const T* __restrict__ w, int n, int k, const unsigned* __restrict__ amax_bits,
                                     uint8_t* __restrict__ nibbles, uint8_t* __restrict__ scales,
                                     float* __restrict__ global_scale) {
   const int e = blockIdx.y;
@@ -93,13 +123,8 @@ __global__ void quant_groups_kernel(const float* __restrict__ w, int n, int k, c
   for (size_t gi = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; gi < groups;
        gi += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const size_t base = (static_cast<size_t>(e) * n * k) + gi * 16;
-    const float4* src = reinterpret_cast<const float4*>(w + base);
     float v[16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 f = src[i];
-      v[4 * i] = f.x, v[4 * i + 1] = f.y, v[4 * i + 2] = f.z, v[4 * i + 3] = f.w;
-    }
+    load16(w + base, v);
     float bmax = 0.f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));

@@ -207,6 +207,23 @@ struct WeightMaps {
   CUtensorMap sh[4];  // the shared expert of a MoE layer (unused otherwise)
 };
 
+// The f16 pairs h[0..3] of columns 8*c8 .. 8*c8+7 (pair e = columns 2e, 2e+1,
+// low half first) of a staged row at rowp: the m16n8k16 B-fragment order (MMA)
+// or pair order (CUDA cores) of their 64-column chunk.
+template <bool kMMA>
+__device__ __forceinline__ void place8(uint8_t* rowp, int c8, const uint32_t (&h)[4]) {
+  const int kcl = c8 >> 3, c64 = (c8 & 7) * 8;  // chunk, first column within the chunk
+  uint8_t* cp = rowp + kcl * kXChunkBytes;
+  if constexpr (kMMA) {
+    // columns c64..c64+7 = k-step kt, half hf, pairs t = 0..3 -> word 8t + 2kt + hf
+    uint32_t* dst = reinterpret_cast<uint32_t*>(cp) + (c64 >> 4) * 2 + ((c64 >> 3) & 1);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) dst[t * 8] = h[t];
+  } else {
+    *reinterpret_cast<uint4*>(cp + c64 * 2) = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+}
+
 // Stage `nrows` bf16 rows of x (row_src[j] = source row, row length k) over
 // columns [col0, col0 + 64*nchunks) into shared memory as f16, row j rescaled by
 // 2^sigma[j] (sigma from the row's amax over the same columns, see
@@ -244,16 +261,7 @@ __device__ __forceinline__ void stage_rows(const uint16_t* __restrict__ x, int k
       const float lo = __uint_as_float(w4[e] << 16) * sc, hi = __uint_as_float(w4[e] & 0xFFFF0000u) * sc;
       h[e] = static_cast<uint32_t>(f32_to_f16_bits(lo)) | (static_cast<uint32_t>(f32_to_f16_bits(hi)) << 16);
     }
-    const int kcl = c8 >> 3, c64 = (c8 & 7) * 8;  // chunk, first column within the chunk
-    uint8_t* cp = rowp + kcl * kXChunkBytes;
-    if constexpr (kMMA) {
-      // columns c64..c64+7 = k-step kt, half hf, pairs t = 0..3 -> word 8t + 2kt + hf
-      uint32_t* dst = reinterpret_cast<uint32_t*>(cp) + (c64 >> 4) * 2 + ((c64 >> 3) & 1);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) dst[t * 8] = h[t];
-    } else {
-      *reinterpret_cast<uint4*>(cp + c64 * 2) = make_uint4(h[0], h[1], h[2], h[3]);
-    }
+    place8<kMMA>(rowp, c8, h);
   };
   for (int row = warp; row <= nrows; row += nwarps) {
     uint8_t* rowp = xs + static_cast<size_t>(row) * stride;
@@ -303,6 +311,46 @@ __device__ __forceinline__ void stage_rows(const uint16_t* __restrict__ x, int k
     }
   }
   after_loads();
+  __syncthreads();
+}
+
+// The same staging for activations already quantized to NVFP4 (the W4A4
+// products): canonical codes [rows, k/2] and E4M3 scales [rows, k/16] of row
+// row_src[j], each 16-column group dequantized as e2m1 * e4m3 * 2^-8 in f16 --
+// exact, as for the weights (at most 6 significant bits, within f16's range) --
+// and sigma[j] = -8, so that the epilogue's 2^(8 - sigma) restores the 2^-8;
+// the row's global scale is applied by the caller's multiplier.
+template <bool kMMA, typename F>
+__device__ __forceinline__ void stage_rows_fp4(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scl,
+                                               int k, int col0, int nchunks, int nrows, const int* row_src,
+                                               int* sigma, uint8_t* xs, int stride, F&& after_loads) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  const int groups = nchunks * 8;  // 8-column groups per row
+  after_loads();  // the rows are read once, with nothing to overlap: issue the copies first
+  for (int row = warp; row <= nrows; row += nwarps) {
+    uint8_t* rowp = xs + static_cast<size_t>(row) * stride;
+    if (row == nrows) {  // the zero row
+      for (int b = lane * 16; b < nchunks * kXChunkBytes; b += 32 * 16) *reinterpret_cast<uint4*>(rowp + b) = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint8_t* crow = codes + static_cast<size_t>(row_src[row]) * (k / 2) + col0 / 2;
+    const uint8_t* srow = scl + static_cast<size_t>(row_src[row]) * (k / 16) + col0 / 16;
+    const int lim = k - col0;  // columns of this row that exist
+    for (int c8 = lane; c8 < groups; c8 += 32) {
+      uint32_t h[4] = {0u, 0u, 0u, 0u};
+      if (c8 * 8 < lim) {
+        const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(crow + c8 * 4));
+        const uint32_t sb = __ldg(srow + (c8 >> 1));
+        e2m1x8_to_f16x2(w, h);
+        const uint32_t s2 = scale_pair_lohi<0, 0>(sb);  // [e4m3, e4m3] * 2^-8
+#pragma unroll
+        for (int e = 0; e < 4; ++e) h[e] = hmul2(h[e], s2);
+      }
+      place8<kMMA>(rowp, c8, h);
+    }
+    if (lane == 0) sigma[row] = -8;
+  }
   __syncthreads();
 }
 

@@ -194,3 +194,12 @@ def test_host_repack_rejects_bad_arguments(so):
     assert so.nvfp4_repack_host(buf, buf, 1, 40, 64, 1, buf, 64) != 0                     # gated n % 64
     assert so.nvfp4_repack_host(buf, buf, 1, 16, 64, 4, buf, 64) != 0                     # unknown flag
     assert so.nvfp4_repack_host(buf, buf, 1, 16, 64, 0, small, 16) != 0                   # out too small
+
+
+def test_w4a4_calls_reject_bad_arguments_before_launch(so):
+    buf = (ctypes.c_uint8 * 256)()
+    ws = (ctypes.c_uint8 * 256)()
+    assert so.nvfp4_quantize_act(None, 2, 64, buf, buf, buf, ws, 256, None) == 1           # null x
+    assert so.nvfp4_quantize_act(buf, 2, 60, buf, buf, buf, ws, 256, None) != 0            # k % 16
+    assert so.nvfp4_quantize_act(buf, 5000, 64, buf, buf, buf, ws, 256, None) != 0         # m > 4096
+    assert so.nvfp4_quantize_act(buf, 2, 64, buf, buf, buf, ws, 0, None) != 0              # workspace
