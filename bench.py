@@ -302,6 +302,17 @@ def time_isolated(lib, wl, calls_m, m, dev, stream, reps=40):
     variants["moe"] = [lib.plan_moe(bufs["x_moe"], bufs["logits"], W.TOP_K, g, d, wl["sh_gate_up"], wl["sh_down"],
                                     route, bufs["moe_out"], stream) for g, d in zip(gus, dns)]
     variants["lm_head"] = [lib.plan_lm_head(wl["lm_head"], bufs["x_lm"], bufs["max"], bufs["argmax"], stream)]
+    out = time_variants(variants, stream, reps)
+    variants.clear()
+    torch.cuda.empty_cache()
+    return out
+
+
+def time_variants(variants, stream, reps):
+    """us per launch of each named list of callables, cycled `reps` times back to back
+    with events around the run on the launching stream (median of 3 runs)."""
+    import torch
+    out = {}
     for name, fns in variants.items():
         with torch.cuda.stream(stream):
             for i in range(4):
@@ -318,10 +329,35 @@ def time_isolated(lib, wl, calls_m, m, dev, stream, reps=40):
             stream.synchronize()
             runs.append(1e3 * e0.elapsed_time(e1) / reps)
         out[name] = statistics.median(runs)
-        del fns
+    return out
+
+
+def time_w4a4(lib, wl, bufs, m, dev, stream, reps=40):
+    """The W4A4 products (activations quantized to NVFP4 per token row) at the step's
+    M: the activation quantizer, the dense GEMMs (rotating over weight copies that
+    together exceed 4x L2) and the lm_head argmax, each alone, back to back."""
+    import torch
+    from nvfp4_w4a16_moe_skinny_gb300 import binding
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    xq_d, xq_l = lib.quantize_act(bufs["x_dense"]), lib.quantize_act(bufs["x_lm"])
+    variants = {"quantize_act_4096": [lib.plan_quantize_act(bufs["x_dense"], xq_d, stream)],
+                "quantize_act_2816": [lib.plan_quantize_act(bufs["x_lm"], xq_l, stream)]}
+    for name, (n, w) in zip(("dense_4096", "dense_14336"), wl["dense"]):
+        copies = [w] + [binding.Weight(w.data.clone(), w.global_scale.clone(), w.n, w.k, 1, 0)
+                        for _ in range(max(1, -(-4 * l2 // w.data.numel())) - 1)]
+        y = bufs["y_4096"] if n == 4096 else bufs["y_14336"]
+        variants[name] = [lib.plan_gemm_w4a4(c, xq_d, y, stream) for c in copies]
+    variants["lm_head"] = [lib.plan_lm_head_w4a4(wl["lm_head"], xq_l, bufs["max"], bufs["argmax"], stream)]
+    us = time_variants(variants, stream, reps)
     variants.clear()
     torch.cuda.empty_cache()
-    return out
+    if lib.device_error() != 0:
+        raise RuntimeError("device error flag set during the W4A4 timing")
+    peak, _ = peaks()
+    b = step_bytes(0)
+    gbs = {k: round(b[k] / (v * 1e-6) / 1e9, 1) for k, v in us.items() if k in b}
+    return {"m": m, "kernels_us": {k: round(v, 2) for k, v in us.items()}, "kernels_gbs": gbs,
+            "kernels_hbm_frac": {k: round(v / peak, 4) for k, v in gbs.items()}}
 
 
 def measure_m(lib, wl, m, args, dev, stream, dist, world, clocks):
@@ -450,6 +486,7 @@ def run_ours(args, rank, world, dist):
         prefill = time_prefill(lib, wl, args, dev, stream) if args.prefill_m > 0 else None
         bufs, _, _, _, _ = make_step(lib, wl, MEASURE_M[0], dev, stream)
         sampling = time_sampling(lib, wl, bufs, MEASURE_M[0], args, dev, stream)
+        w4a4 = time_w4a4(lib, wl, bufs, MEASURE_M[0], dev, stream)
     head = per_m[MEASURE_M[0]]
     peak, peak_kind = peaks()
     lm_bytes = head["bytes"]["lm_head"]
@@ -491,6 +528,7 @@ def run_ours(args, rank, world, dist):
         "graph_ms_per_step": head["graph_ms_per_step"],
         "prefill": prefill,
         "lm_head_sample": sampling,
+        "w4a4": w4a4,
         "gpu_launches": head["launches_per_step"] * args.steps,
         "timing": "ms_per_step: median over 20 batches of back-to-back steps (events at batch boundaries only); "
                   "roofline: events around the lm_head in a second pass over the same steps; kernels_us: each "

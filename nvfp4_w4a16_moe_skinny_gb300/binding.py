@@ -379,6 +379,53 @@ class Library:
         run.keep = (cw, ws)
         return run
 
+    def plan_quantize_act(self, x: torch.Tensor, out, stream=None):
+        """nvfp4_quantize_act as a zero-argument callable into `out` = (codes, scales, g)."""
+        m, k = x.shape
+        ws = self.workspace("quantize_act", max(16, self.lib.nvfp4_quantize_workspace_bytes(m)), x.device)
+        args = (x.data_ptr(), m, k, out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(), ws.data_ptr(),
+                ws.numel(), _stream(stream))
+        fn = self.lib.nvfp4_quantize_act
+
+        def run():
+            st = fn(*args)
+            if st:
+                raise NVFP4Error("nvfp4_quantize_act", st)
+        run.keep = (ws,)
+        return run
+
+    def plan_gemm_w4a4(self, w: Weight, xq, y: torch.Tensor, stream=None):
+        codes, scales, g = xq
+        m = codes.shape[0]
+        ws = self.workspace("gemm", self.lib.nvfp4_gemm_workspace_bytes(m, w.n, w.k), codes.device)
+        cw = w.c()
+        args = (ctypes.byref(cw), codes.data_ptr(), scales.data_ptr(), g.data_ptr(), m, y.data_ptr(), ws.data_ptr(),
+                ws.numel(), _stream(stream))
+        fn = self.lib.nvfp4_gemm_w4a4
+
+        def run():
+            st = fn(*args)
+            if st:
+                raise NVFP4Error("nvfp4_gemm_w4a4", st)
+        run.keep = (cw, ws)
+        return run
+
+    def plan_lm_head_w4a4(self, w: Weight, xq, max_logit: torch.Tensor, argmax: torch.Tensor, stream=None):
+        codes, scales, g = xq
+        m = codes.shape[0]
+        ws = self.workspace("lm_head", self.lib.lm_head_workspace_bytes(m, w.n), codes.device)
+        cw = w.c()
+        args = (ctypes.byref(cw), codes.data_ptr(), scales.data_ptr(), g.data_ptr(), m, max_logit.data_ptr(),
+                argmax.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream))
+        fn = self.lib.lm_head_argmax_w4a4
+
+        def run():
+            st = fn(*args)
+            if st:
+                raise NVFP4Error("lm_head_argmax_w4a4", st)
+        run.keep = (cw, ws)
+        return run
+
     def plan_lm_head(self, w: Weight, x: torch.Tensor, max_logit: torch.Tensor, argmax: torch.Tensor, stream=None):
         m = x.shape[0]
         ws = self.workspace("lm_head", self.lib.lm_head_workspace_bytes(m, w.n), x.device)

@@ -402,9 +402,16 @@ nvfp4_status nvfp4_quantize(const float* w, int32_t num_matrices, int32_t n, int
 
 nvfp4_status nvfp4_quantize_act(const uint16_t* x, int32_t m, int32_t k, uint8_t* codes, uint8_t* scales,
                                 float* global_scale, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  if (m > 4096) return NVFP4_ERR_SHAPE;
-  // each token row is a matrix of its own: one global scale per row
-  return quantize_launch(x, m, 1, k, codes, scales, global_scale, ws, ws_bytes, stream);
+  // each token row is a matrix of its own (one global scale per row): one grid,
+  // one CTA per row; the workspace is not needed but checked as for nvfp4_quantize
+  if (!x || !codes || !scales || !global_scale) return NVFP4_ERR_NULL;
+  if (m < 1 || m > 4096 || k < 16 || (k % 16)) return NVFP4_ERR_SHAPE;
+  if (!ws || ws_bytes < nvfp4_quantize_workspace_bytes(m)) return NVFP4_ERR_WORKSPACE;
+  if (!aligned(x, 16) || !aligned(codes, 8) || !aligned(global_scale, 4)) return NVFP4_ERR_ALIGN;
+  if (launch_pdl(quant_act_rows_kernel, dim3(m), dim3(kActQuantThreads), 0, stream, x, static_cast<int>(k), codes,
+                 scales, global_scale) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  return launched();
 }
 
 nvfp4_status nvfp4_repack(const uint8_t* nibbles, const uint8_t* scales, int32_t num_matrices, int32_t n, int32_t k,

@@ -109,6 +109,57 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
   return (c & 0x80) ? -mag : mag;
 }
 
+// One 16-element group under global scale g: its E4M3 scale code and its eight
+// code bytes (two words, column 2i in the low nibble of byte i).
+//
+// The scale code comes from one float64 division (the exact quotient's
+// decision, as above).  An element's code is the E2M1 rounding of the exact
+// quotient w / d, d = e4m3(s) * g; it is taken in fp32 where that is provably the
+// same: q = |w| * fp32(1/d) is within 2^-23 (relative) of the exact quotient, so
+// the exact quotient lies in [q (1 - 2^-20), q (1 + 2^-20)] (both products
+// rounded in fp32, still enclosing it); rounding is monotonic, so when both ends
+// round to the same code that code is the exact quotient's.  Otherwise (a
+// quotient within 2^-20 of a rounding midpoint) the element takes the float64
+// division.
+__device__ __forceinline__ void quantize_group16(const float (&v)[16], float g, uint32_t& s_code,
+                                                 uint32_t (&packed)[2]) {
+  float bmax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+  s_code = 0;
+  double denom = 0.0;
+  if (g > 0.f) {
+    const double t = static_cast<double>(bmax) / (6.0 * static_cast<double>(g));  // exact divisor
+    s_code = e4m3_code_rne(f64_to_f32_round_odd(t));
+    denom = static_cast<double>(e4m3_value(s_code)) * static_cast<double>(g);      // exact product
+  }
+  packed[0] = packed[1] = 0u;
+  if (!(denom > 0.0)) return;
+  const float inv = static_cast<float>(1.0 / denom);
+  const bool fast = inv < 1e30f;  // (an fp32 1/d far from overflow)
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float lo = v[2 * i], hi = v[2 * i + 1];
+    uint32_t code = 0;
+    bool exact = !fast;
+    if (fast) {
+      const float ql = fabsf(lo) * inv, qh = fabsf(hi) * inv;
+      const uint32_t c_dn = e2m1x2_code_rne(ql * 0.99999904632568359375f, qh * 0.99999904632568359375f);
+      const uint32_t c_up = e2m1x2_code_rne(ql * 1.00000095367431640625f, qh * 1.00000095367431640625f);
+      exact = c_dn != c_up;
+      code = c_dn;
+    }
+    if (exact) {
+      const float ql = f64_to_f32_round_odd(fabs(static_cast<double>(lo)) / denom);
+      const float qh = f64_to_f32_round_odd(fabs(static_cast<double>(hi)) / denom);
+      code = e2m1x2_code_rne(ql, qh);
+    }
+    // the signs of w (kept for codes that round to zero)
+    code |= ((__float_as_uint(lo) >> 31) << 3) | ((__float_as_uint(hi) >> 31) << 7);
+    packed[i >> 2] |= code << (8 * (i & 3));
+  }
+}
+
 // One thread per 16-element group.
 template <typename T>
 __global__ void quant_groups_kernel(const T* __restrict__ w, int n, int k, const unsigned* __restrict__ amax_bits,
@@ -122,31 +173,55 @@ __global__ void quant_groups_kernel(const T* __restrict__ w, int n, int k, const
   if (blockIdx.x == 0 && threadIdx.x == 0) global_scale[e] = g;
   for (size_t gi = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; gi < groups;
        gi += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t base = (static_cast<size_t>(e) * n * k) + gi * 16;
     float v[16];
-    load16(w + base, v);
-    float bmax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
-    uint32_t s_code = 0;
-    double denom = 0.0;
-    if (g > 0.f) {
-      const double t = static_cast<double>(bmax) / (6.0 * static_cast<double>(g));  // exact divisor
-      s_code = e4m3_code_rne(f64_to_f32_round_odd(t));
-      denom = static_cast<double>(e4m3_value(s_code)) * static_cast<double>(g);      // exact product
-    }
-    uint32_t packed[2] = {0u, 0u};
-    if (denom > 0.0) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float lo = f64_to_f32_round_odd(static_cast<double>(v[2 * i]) / denom);
-        const float hi = f64_to_f32_round_odd(static_cast<double>(v[2 * i + 1]) / denom);
-        packed[i >> 2] |= e2m1x2_code_rne(lo, hi) << (8 * (i & 3));
-      }
-    }
+    load16(w + (static_cast<size_t>(e) * n * k) + gi * 16, v);
+    uint32_t s_code, packed[2];
+    quantize_group16(v, g, s_code, packed);
     uint2* dst = reinterpret_cast<uint2*>(nibbles + (static_cast<size_t>(e) * n * k) / 2 + gi * 8);
     *dst = make_uint2(packed[0], packed[1]);
     scales[static_cast<size_t>(e) * groups + gi] = static_cast<uint8_t>(s_code);
+  }
+}
+
+// Activation rows (bf16 [m, k]) to NVFP4 with one global scale per row, in one
+// grid: CTA r reduces row r's amax, then quantizes its 16-element groups.  The
+// rows may come from the previous grid (programmatic dependent launch).
+constexpr int kActQuantThreads = 256;
+__global__ void __launch_bounds__(kActQuantThreads) quant_act_rows_kernel(
+    const uint16_t* __restrict__ x, int k, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+    float* __restrict__ global_scale) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int r = blockIdx.x;
+  const uint16_t* row = x + static_cast<size_t>(r) * k;
+  const int groups = k / 16;
+  // the row's amax, 16 elements (two 16-byte loads) per thread and step
+  unsigned best = 0;  // as in quant_amax_kernel: the largest |x| bit pattern
+  for (int gi = threadIdx.x; gi < groups; gi += blockDim.x) {
+    float v[16];
+    load16(row + gi * 16, v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) best = max(best, __float_as_uint(fabsf(v[i])));
+  }
+  for (int off = 16; off > 0; off >>= 1) {
+    const unsigned o = __shfl_xor_sync(0xffffffffu, best, off);
+    best = o > best ? o : best;
+  }
+  __shared__ unsigned warp_best[kActQuantThreads / 32];
+  if ((threadIdx.x & 31) == 0) warp_best[threadIdx.x >> 5] = best;
+  __syncthreads();
+  unsigned amax = 0;
+#pragma unroll
+  for (int i = 0; i < kActQuantThreads / 32; ++i) amax = warp_best[i] > amax ? warp_best[i] : amax;
+  const float g = __fdiv_rn(__uint_as_float(amax), 2688.0f);
+  if (threadIdx.x == 0) global_scale[r] = g;
+  for (int gi = threadIdx.x; gi < groups; gi += blockDim.x) {
+    float v[16];
+    load16(row + gi * 16, v);
+    uint32_t s_code, packed[2];
+    quantize_group16(v, g, s_code, packed);
+    *reinterpret_cast<uint2*>(codes + static_cast<size_t>(r) * (k / 2) + gi * 8) = make_uint2(packed[0], packed[1]);
+    scales[static_cast<size_t>(r) * groups + gi] = static_cast<uint8_t>(s_code);
   }
 }
 
