@@ -34,17 +34,11 @@ template <int kEpi>
 nvfp4_status dispatch_stream(const Job& p, const WeightMaps& maps, const Plan& plan, cudaStream_t stream) {
   if constexpr (kEpi == kEpiGated || kEpi == kEpiRows)
     if (plan.per_run) return launch_planned(prefill_kernel<kEpi>, p, maps, plan, stream);
-  switch (p.m) {
-    case 1: return launch_stream<1, false, kEpi>(p, maps, plan, stream);
-    case 2: return launch_stream<2, false, kEpi>(p, maps, plan, stream);
-    case 3: return launch_stream<3, false, kEpi>(p, maps, plan, stream);
-    case 4: return launch_stream<4, false, kEpi>(p, maps, plan, stream);
-    case 5: return launch_stream<5, false, kEpi>(p, maps, plan, stream);
-    case 6: return launch_stream<6, false, kEpi>(p, maps, plan, stream);
-    case 7: return launch_stream<7, false, kEpi>(p, maps, plan, stream);
-    case 8: return launch_stream<8, true, kEpi>(p, maps, plan, stream);
-    default: return launch_stream<16, true, kEpi>(p, maps, plan, stream);
-  }
+  // one token: CUDA cores with a warp-shuffle reduction; 2..8 tokens: one 8-slot
+  // tensor-core column (empty slots read a zero row); 9..16: two columns
+  if (p.m == 1) return launch_stream<1, false, kEpi>(p, maps, plan, stream);
+  if (p.m <= 8) return launch_stream<8, true, kEpi>(p, maps, plan, stream);
+  return launch_stream<16, true, kEpi>(p, maps, plan, stream);
 }
 
 template <int kEpi>

@@ -61,7 +61,7 @@ constexpr int kPlanSMs = 152;
 constexpr int kMaxSplit = 16;
 
 
-bool use_mma(int m) { return m >= 8; }
+bool use_mma(int m) { return m >= 2; }  // (the decode kernel's instance for m; see dispatch_stream)
 // accumulator floats per lane and 16-row tile (the fixup partial of one tile)
 int acc_per_tile(int m) { return use_mma(m) ? (m <= 8 ? 4 : 8) : 2 * m; }
 
