@@ -175,8 +175,9 @@ nvfp4_status nvfp4_repack_host(const uint8_t *nibbles, const uint8_t *scales, in
  *       uses this workspace (for example cudaMemsetAsync once after
  *       allocation); every completed call leaves them zero again, so the same
  *       workspace may serve calls of any shape whose size it covers.
- * M = 1..7 runs on CUDA cores (warp-shuffle reduction); M = 8..16 on m16n8k16
- * tensor-core MMAs with the weights as the 16-row operand.
+ * M = 1 runs on CUDA cores (warp-shuffle reduction); M = 2..16 on m16n8k16
+ * tensor-core MMAs with the weights as the 16-row operand and the tokens in one
+ * (M <= 8) or two 8-slot columns.
  */
 size_t nvfp4_gemm_workspace_bytes(int32_t m, int32_t n, int32_t k);
 nvfp4_status nvfp4_gemm(const nvfp4_weight *w, const uint16_t *x, int32_t m, uint16_t *y, void *ws,

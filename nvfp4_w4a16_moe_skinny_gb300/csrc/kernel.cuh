@@ -516,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kStep = copy_chunks(TN);
         int ch = 0;
         if constexpr (kStep == 1 && !kMMA) {
-          // CUDA cores (M <= 7, issue-bound): whole chunks two at a time -- both
+          // CUDA cores (one token, issue-bound): whole chunks two at a time -- both
           // stages' waits, both chunks, both refills -- halving the per-chunk
           // wait and refill work.  Only with 4+ stages, so that two stay in flight
           // while the pair is consumed.  (The tensor-core path measured slower so.)

@@ -22,12 +22,12 @@
 //    The x fragments of the 64 columns are loaded once and feed the TN tiles.
 //    Each E2M1 pair goes through the hardware converter and is multiplied in f16
 //    by its E4M3 scale (exact: the product has at most 6 significant bits).
-//  * core_chunk<MT, TN>: CUDA cores for up to 7 tokens.  Lane (g, q) takes rows
-//    g and g+8 of each tile over the 16-column group q; it sums E2M1 x
-//    activation products in f32 (mixed-precision FMA; the products are exact)
-//    and scales each group sum once (MT <= 2), or scales the weights in f16
-//    first and accumulates directly (MT >= 3, fewer live registers).  The
-//    cross-lane sum over q is left to warp shuffles in the epilogue.
+//  * core_chunk<TN>: CUDA cores for one token.  Lane (g, q) takes rows g and
+//    g+8 of each tile over the 16-column group q; it sums E2M1 x activation
+//    products in f32 (mixed-precision FMA; the products are exact) and scales
+//    each group sum once.  The cross-lane sum over q is left to warp shuffles in
+//    the epilogue.  (Two or more tokens run on an 8-slot tensor-core column:
+//    one FMA per weight and token cost more than the MMA from two tokens up.)
 #pragma once
 
 #include "common.cuh"
@@ -112,84 +112,40 @@ struct CoreLane {
   }
 };
 
-// TN tiles at `st` on CUDA cores.  xr[m]: token m's staged row for this chunk.
-// acc[r][m][0] = tile r, row g; acc[r][m][1] = row g+8 (partial over group q).
+// TN tiles at `st` on CUDA cores for one token (MT == 1).  xr[0]: the token's
+// staged row for this chunk.  acc[r][0][0] = tile r, row g; acc[r][0][1] = row
+// g+8 (partial over group q).
 template <int MT, int TN>
 __device__ __forceinline__ void core_chunk(uint32_t st, const uint32_t (&xr)[MT], const CoreLane& cl,
                                            float (&acc)[4][MT][2]) {
-  if constexpr (MT <= 2) {
-    uint32_t xw[MT][4][2];
+  static_assert(MT == 1, "the CUDA-core consumer serves one token");
+  uint32_t xw[4][2];
 #pragma unroll
-    for (int m = 0; m < MT; ++m)
+  for (int j = 0; j < 4; ++j) {
+    xw[j][0] = lds32(xr[0] + cl.x_off[j]);
+    xw[j][1] = lds32(xr[0] + cl.x_off[j] + 16);
+  }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        xw[m][j][0] = lds32(xr[m] + cl.x_off[j]);
-        xw[m][j][1] = lds32(xr[m] + cl.x_off[j] + 16);
-      }
-#pragma unroll
-    for (int r = 0; r < TN; ++r) {
-      const uint32_t tile = st + r * kTileBytes;
-      const uint32_t sp = scale_pair_lohi<0, 1>(lds16(tile + cl.s_off));
-      float pa[MT], pb[MT], pc[MT], pd[MT];
-#pragma unroll
-      for (int m = 0; m < MT; ++m) pa[m] = pb[m] = pc[m] = pd[m] = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t hh[4];
-        e2m1x8_to_f16x2(lds32(tile + cl.w_off[j]), hh);
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          pa[m] = fma_f16lo(hh[0], xw[m][j][0], pa[m]);
-          pb[m] = fma_f16hi(hh[0], xw[m][j][0], pb[m]);
-          pa[m] = fma_f16lo(hh[2], xw[m][j][1], pa[m]);
-          pb[m] = fma_f16hi(hh[2], xw[m][j][1], pb[m]);
-          pc[m] = fma_f16lo(hh[1], xw[m][j][0], pc[m]);
-          pd[m] = fma_f16hi(hh[1], xw[m][j][0], pd[m]);
-          pc[m] = fma_f16lo(hh[3], xw[m][j][1], pc[m]);
-          pd[m] = fma_f16hi(hh[3], xw[m][j][1], pd[m]);
-        }
-      }
-      const float sg = f16lo_to_f32(sp), sg8 = f16hi_to_f32(sp);  // scale * 2^-8
-#pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        acc[r][m][0] = fmaf(pa[m] + pb[m], sg, acc[r][m][0]);
-        acc[r][m][1] = fmaf(pc[m] + pd[m], sg8, acc[r][m][1]);
-      }
-    }
-  } else {
-    uint32_t sgd[TN];  // (scale row g, scale row g+8) * 2^-8 per tile
-#pragma unroll
-    for (int r = 0; r < TN; ++r) sgd[r] = scale_pair_lohi<0, 1>(lds16(st + r * kTileBytes + cl.s_off));
+  for (int r = 0; r < TN; ++r) {
+    const uint32_t tile = st + r * kTileBytes;
+    const uint32_t sp = scale_pair_lohi<0, 1>(lds16(tile + cl.s_off));
+    float pa = 0.f, pb = 0.f, pc = 0.f, pd = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      uint32_t x0[MT], x1[MT];
-#pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        x0[m] = lds32(xr[m] + cl.x_off[j]);
-        x1[m] = lds32(xr[m] + cl.x_off[j] + 16);
-      }
-#pragma unroll
-      for (int r = 0; r < TN; ++r) {
-        uint32_t hh[4];
-        e2m1x8_to_f16x2(lds32(st + r * kTileBytes + cl.w_off[j]), hh);
-        uint32_t h0, h1, h2, h3;
-        hmul2_bcast(hh[0], hh[1], sgd[r], h0, h1);
-        hmul2_bcast(hh[2], hh[3], sgd[r], h2, h3);
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          float a0 = acc[r][m][0], a1 = acc[r][m][1];
-          a0 = fma_f16lo(h0, x0[m], a0);
-          a0 = fma_f16hi(h0, x0[m], a0);
-          a0 = fma_f16lo(h2, x1[m], a0);
-          a0 = fma_f16hi(h2, x1[m], a0);
-          a1 = fma_f16lo(h1, x0[m], a1);
-          a1 = fma_f16hi(h1, x0[m], a1);
-          a1 = fma_f16lo(h3, x1[m], a1);
-          a1 = fma_f16hi(h3, x1[m], a1);
-          acc[r][m][0] = a0, acc[r][m][1] = a1;
-        }
-      }
+      uint32_t hh[4];
+      e2m1x8_to_f16x2(lds32(tile + cl.w_off[j]), hh);
+      pa = fma_f16lo(hh[0], xw[j][0], pa);
+      pb = fma_f16hi(hh[0], xw[j][0], pb);
+      pa = fma_f16lo(hh[2], xw[j][1], pa);
+      pb = fma_f16hi(hh[2], xw[j][1], pb);
+      pc = fma_f16lo(hh[1], xw[j][0], pc);
+      pd = fma_f16hi(hh[1], xw[j][0], pd);
+      pc = fma_f16lo(hh[3], xw[j][1], pc);
+      pd = fma_f16hi(hh[3], xw[j][1], pd);
     }
+    const float sg = f16lo_to_f32(sp), sg8 = f16hi_to_f32(sp);  // scale * 2^-8
+    acc[r][0][0] = fmaf(pa + pb, sg, acc[r][0][0]);
+    acc[r][0][1] = fmaf(pc + pd, sg8, acc[r][0][1]);
   }
 }
 
