@@ -332,6 +332,33 @@ def time_variants(variants, stream, reps):
     return out
 
 
+def time_m_sweep(lib, wl, dev, stream, reps=40):
+    """The lm_head and the N=4096 dense GEMM alone at every M = 1..16 (back to back,
+    dense weights rotating over copies that exceed 4x L2): us per launch."""
+    import torch
+    from nvfp4_w4a16_moe_skinny_gb300 import binding
+    from nvfp4_w4a16_moe_skinny_gb300 import workloads as W
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    (n0, w0), _ = wl["dense"]
+    copies = [w0] + [binding.Weight(w0.data.clone(), w0.global_scale.clone(), w0.n, w0.k, 1, 0)
+                     for _ in range(max(1, -(-4 * l2 // w0.data.numel())) - 1)]
+    out = {}
+    for m in range(1, 17):
+        xl = torch.from_numpy(W.LMHeadCase(m=m).x()[0].view(np.int16)).to(dev).view(torch.bfloat16)
+        xd = torch.from_numpy(W.DenseCase.sweep(m, n0).x()[0].view(np.int16)).to(dev).view(torch.bfloat16)
+        mx = torch.empty((m,), dtype=torch.float32, device=dev)
+        am = torch.empty((m,), dtype=torch.int32, device=dev)
+        y = torch.empty((m, n0), dtype=torch.bfloat16, device=dev)
+        us = time_variants({"lm_head": [lib.plan_lm_head(wl["lm_head"], xl, mx, am, stream)],
+                            "dense_4096": [lib.plan_gemm(c, xd, y, stream) for c in copies]}, stream, reps)
+        out[str(m)] = {k: round(v, 2) for k, v in us.items()}
+    del copies
+    torch.cuda.empty_cache()
+    if lib.device_error() != 0:
+        raise RuntimeError("device error flag set during the M sweep")
+    return out
+
+
 def time_w4a4(lib, wl, bufs, m, dev, stream, reps=40):
     """The W4A4 products (activations quantized to NVFP4 per token row) at the step's
     M: the activation quantizer, the dense GEMMs (rotating over weight copies that
@@ -487,6 +514,7 @@ def run_ours(args, rank, world, dist):
         bufs, _, _, _, _ = make_step(lib, wl, MEASURE_M[0], dev, stream)
         sampling = time_sampling(lib, wl, bufs, MEASURE_M[0], args, dev, stream)
         w4a4 = time_w4a4(lib, wl, bufs, MEASURE_M[0], dev, stream)
+        m_sweep = time_m_sweep(lib, wl, dev, stream)
     head = per_m[MEASURE_M[0]]
     peak, peak_kind = peaks()
     lm_bytes = head["bytes"]["lm_head"]
@@ -529,6 +557,7 @@ def run_ours(args, rank, world, dist):
         "prefill": prefill,
         "lm_head_sample": sampling,
         "w4a4": w4a4,
+        "m_sweep_us": m_sweep,
         "gpu_launches": head["launches_per_step"] * args.steps,
         "timing": "ms_per_step: median over 20 batches of back-to-back steps (events at batch boundaries only); "
                   "roofline: events around the lm_head in a second pass over the same steps; kernels_us: each "
