@@ -649,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < NI; ++i) sum[c][i] = 0.f;
           const float* src0 = p.fix + ((cell0 + a) * p.S * 32 + lane) * V;
-          constexpr int kBatch = V >= 12 ? 1 : (V >= 8 ? 2 : 4);  // slices in flight together (registers)
+          constexpr int kBatch = V >= 8 ? 2 : 8;  // slices in flight together (registers)
           for (int s0 = 0; s0 < p.S; s0 += kBatch) {
             float buf[kBatch][NA][NI];
 #pragma unroll
