@@ -304,6 +304,22 @@ nvfp4_status moe_ffn_grouped(const uint16_t *x, int32_t m, int32_t top_k, const 
                              uint16_t *out, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * One MoE layer in one call (gemma-cuda-hybrid README, "Everything it has /
+ * Inference engine": the router's top-k, then the routed and shared experts'
+ * SwiGLU FFNs, weighted and summed): moe_route_topk_ex (route_flags,
+ * expert_scale as there) writing ids, probs, expert_offsets and sorted_pairs,
+ * then moe_ffn_grouped on them, with the same results and workspace as the two
+ * calls made in turn.  The number of experts is gate_up->num_matrices; logits is
+ * [m, num_matrices] fp32.  All arguments of both steps are checked before the
+ * first launch, so an error status means nothing was launched.
+ */
+nvfp4_status moe_forward(const uint16_t *x, const float *logits, int32_t m, int32_t top_k, int32_t route_flags,
+                         const float *expert_scale, int32_t *ids, float *probs, int32_t *expert_offsets,
+                         int32_t *sorted_pairs, const nvfp4_weight *gate_up, const nvfp4_weight *down,
+                         const nvfp4_weight *shared_gate_up, const nvfp4_weight *shared_down, uint16_t *out, void *ws,
+                         size_t ws_bytes, cudaStream_t stream);
+
+/*
  * lm_head with fused greedy argmax: for each token row m, max_n (W_hat . x_m)[n]
  * in fp32 and the lowest n reaching it.  The vocabulary is split across CTAs
  * and K across the warps of a CTA; no logits are written to memory.

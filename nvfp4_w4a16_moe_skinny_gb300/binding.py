@@ -17,6 +17,7 @@ import torch
 from .build import LIB
 
 NVFP4_GATED = 1
+NVFP4_ROUTE_SOFTMAX_ALL = 1
 LAYOUT_VERSION = 2
 
 STATUS = {0: "ok", 1: "null pointer", 2: "bad shape", 3: "misaligned pointer",
@@ -28,7 +29,7 @@ EXPORTS = (
     "nvfp4_gemm", "moe_route_topk", "moe_ffn_workspace_bytes", "moe_ffn_grouped",
     "lm_head_workspace_bytes", "lm_head_argmax", "lm_head_argmax_noalloc", "nvfp4_plan_info",
     "lm_head_sample", "moe_route_topk_ex", "lm_head_sample_ex", "nvfp4_plan_check", "moe_router_logits",
-    "nvfp4_repack_host", "nvfp4_quantize_act", "nvfp4_gemm_w4a4", "lm_head_argmax_w4a4",
+    "nvfp4_repack_host", "nvfp4_quantize_act", "nvfp4_gemm_w4a4", "lm_head_argmax_w4a4", "moe_forward",
 )
 
 
@@ -106,6 +107,10 @@ def _sig(lib):
     lib.lm_head_sample_ex.restype = ctypes.c_int
     lib.moe_router_logits.argtypes = [ctypes.POINTER(CWeight), _P, _I, _P, ctypes.c_float, _P, _P, _SZ, _P]
     lib.moe_router_logits.restype = ctypes.c_int
+    lib.moe_forward.argtypes = [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, ctypes.POINTER(CWeight),
+                                ctypes.POINTER(CWeight), ctypes.POINTER(CWeight), ctypes.POINTER(CWeight), _P, _P, _SZ,
+                                _P]
+    lib.moe_forward.restype = ctypes.c_int
     lib.nvfp4_quantize_act.argtypes = [_P, _I, _I, _P, _P, _P, _P, _SZ, _P]
     lib.nvfp4_quantize_act.restype = ctypes.c_int
     lib.nvfp4_gemm_w4a4.argtypes = [ctypes.POINTER(CWeight), _P, _P, _P, _I, _P, _P, _SZ, _P]
@@ -341,7 +346,7 @@ class Library:
                 pairs.data_ptr(), _stream(stream)))
         else:
             self._check("moe_route_topk_ex", self.lib.moe_route_topk_ex(
-                logits.data_ptr(), m, e, top_k, 1 if softmax_all else 0,
+                logits.data_ptr(), m, e, top_k, NVFP4_ROUTE_SOFTMAX_ALL if softmax_all else 0,
                 expert_scale.data_ptr() if expert_scale is not None else None, ids.data_ptr(), probs.data_ptr(),
                 offsets.data_ptr(), pairs.data_ptr(), _stream(stream)))
         return out
@@ -441,9 +446,36 @@ class Library:
         run.keep = (cw, ws)
         return run
 
+    def moe_forward(self, x, logits, top_k, gate_up: Weight, down: Weight, shared_gate_up: Weight = None,
+                    shared_down: Weight = None, route_out=None, out=None, stream=None, softmax_all: bool = False,
+                    expert_scale: torch.Tensor = None):
+        """The MoE layer in one C call (router + grouped FFN): returns (out, (ids, probs, offsets, pairs))."""
+        m, d = x.shape
+        e = logits.shape[1]
+        dev = x.device
+        if route_out is None:
+            route_out = (torch.empty((m, top_k), dtype=torch.int32, device=dev),
+                         torch.empty((m, top_k), dtype=torch.float32, device=dev),
+                         torch.empty((e + 1,), dtype=torch.int32, device=dev),
+                         torch.empty((m * top_k,), dtype=torch.int32, device=dev))
+        if out is None:
+            out = torch.empty((m, d), dtype=torch.bfloat16, device=dev)
+        ws = self.workspace("moe", self.lib.moe_ffn_workspace_bytes(m, top_k, gate_up.num_matrices, d, down.k), dev)
+        cg, cd = gate_up.c(), down.c()
+        sg = shared_gate_up.c() if shared_gate_up is not None else None
+        sd = shared_down.c() if shared_down is not None else None
+        ids, probs, offsets, pairs = route_out
+        self._check("moe_forward", self.lib.moe_forward(
+            x.data_ptr(), logits.data_ptr(), m, top_k, NVFP4_ROUTE_SOFTMAX_ALL if softmax_all else 0,
+            _ptr(expert_scale), ids.data_ptr(), probs.data_ptr(), offsets.data_ptr(), pairs.data_ptr(),
+            ctypes.byref(cg), ctypes.byref(cd), ctypes.byref(sg) if sg is not None else None,
+            ctypes.byref(sd) if sd is not None else None, out.data_ptr(), ws.data_ptr(), ws.numel(),
+            _stream(stream)))
+        return out, route_out
+
     def plan_moe(self, x, logits, top_k, gate_up: Weight, down: Weight, shared_gate_up: Weight, shared_down: Weight,
                  route_out, out, stream=None):
-        """Router + grouped FFN as one callable (two C calls)."""
+        """The MoE layer (moe_forward: router + grouped FFN in one C call) as a zero-argument callable."""
         m, d = x.shape
         e = logits.shape[1]
         ids, probs, offsets, pairs = route_out
@@ -453,20 +485,16 @@ class Library:
         sg = shared_gate_up.c() if shared_gate_up is not None else None
         sd = shared_down.c() if shared_down is not None else None
         s = _stream(stream)
-        rargs = (logits.data_ptr(), m, e, top_k, ids.data_ptr(), probs.data_ptr(), offsets.data_ptr(),
-                 pairs.data_ptr(), s)
-        fargs = (x.data_ptr(), m, top_k, probs.data_ptr(), offsets.data_ptr(), pairs.data_ptr(), ctypes.byref(cg),
-                 ctypes.byref(cd), ctypes.byref(sg) if sg is not None else None,
-                 ctypes.byref(sd) if sd is not None else None, out.data_ptr(), ws.data_ptr(), ws.numel(), s)
-        route, ffn = self.lib.moe_route_topk, self.lib.moe_ffn_grouped
+        args = (x.data_ptr(), logits.data_ptr(), m, top_k, 0, None, ids.data_ptr(), probs.data_ptr(),
+                offsets.data_ptr(), pairs.data_ptr(), ctypes.byref(cg), ctypes.byref(cd),
+                ctypes.byref(sg) if sg is not None else None, ctypes.byref(sd) if sd is not None else None,
+                out.data_ptr(), ws.data_ptr(), ws.numel(), s)
+        fn = self.lib.moe_forward
 
         def run():
-            st = route(*rargs)
+            st = fn(*args)
             if st:
-                raise NVFP4Error("moe_route_topk", st)
-            st = ffn(*fargs)
-            if st:
-                raise NVFP4Error("moe_ffn_grouped", st)
+                raise NVFP4Error("moe_forward", st)
         run.keep = (cg, cd, sg, sd, ws)
         return run
 

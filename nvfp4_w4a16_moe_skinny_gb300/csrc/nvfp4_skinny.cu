@@ -741,11 +741,16 @@ size_t moe_ffn_workspace_bytes(int32_t m, int32_t top_k, int32_t n_experts, int3
   return moe_workspace(m, top_k, n_experts, d, inter, true).total;
 }
 
-nvfp4_status moe_ffn_grouped(const uint16_t* x, int32_t m, int32_t top_k, const float* probs,
-                             const int32_t* expert_offsets, const int32_t* sorted_pairs,
-                             const nvfp4_weight* gate_up, const nvfp4_weight* down,
-                             const nvfp4_weight* shared_gate_up, const nvfp4_weight* shared_down, uint16_t* out,
-                             void* ws, size_t ws_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace nvfp4 {
+namespace {
+
+// The grouped FFN's argument checks (no launch).
+nvfp4_status moe_ffn_check(const uint16_t* x, int32_t m, int32_t top_k, const float* probs,
+                           const int32_t* expert_offsets, const int32_t* sorted_pairs, const nvfp4_weight* gate_up,
+                           const nvfp4_weight* down, const nvfp4_weight* shared_gate_up,
+                           const nvfp4_weight* shared_down, const uint16_t* out, const void* ws, size_t ws_bytes) {
   if (!x || !probs || !expert_offsets || !sorted_pairs || !out || !gate_up || !down) return NVFP4_ERR_NULL;
   if ((shared_gate_up == nullptr) != (shared_down == nullptr)) return NVFP4_ERR_NULL;
   const int n_exp = gate_up->num_matrices;
@@ -766,6 +771,21 @@ nvfp4_status moe_ffn_grouped(const uint16_t* x, int32_t m, int32_t top_k, const 
   if (!aligned(x, 16) || !aligned(out, 4) || !aligned(probs, 4)) return NVFP4_ERR_ALIGN;
   if (!ws || ws_bytes < moe_ffn_workspace_bytes(m, top_k, n_exp, d, inter)) return NVFP4_ERR_WORKSPACE;
   if (!aligned(ws, 16)) return NVFP4_ERR_ALIGN;
+  return NVFP4_OK;
+}
+
+// The grouped FFN's launches (gate+up, down, combine) after moe_ffn_check.
+nvfp4_status moe_ffn_launch(const uint16_t* x, int32_t m, int32_t top_k, const float* probs,
+                            const int32_t* expert_offsets, const int32_t* sorted_pairs,
+                            const nvfp4_weight* gate_up, const nvfp4_weight* down,
+                            const nvfp4_weight* shared_gate_up, const nvfp4_weight* shared_down, uint16_t* out,
+                            void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (const nvfp4_status st = moe_ffn_check(x, m, top_k, probs, expert_offsets, sorted_pairs, gate_up, down,
+                                            shared_gate_up, shared_down, out, ws, ws_bytes))
+    return st;
+  const int n_exp = gate_up->num_matrices;
+  const int d = gate_up->k, inter = down->k;
+  const bool shared = shared_gate_up != nullptr;
   const MoESplits sp = moe_splits(m, top_k, n_exp, d, inter, true);
   const MoEWorkspace wl = moe_workspace(m, top_k, n_exp, d, inter, true);
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -819,6 +839,39 @@ nvfp4_status moe_ffn_grouped(const uint16_t* x, int32_t m, int32_t top_k, const 
                  probs, m, top_k, d, shared, out) != cudaSuccess)
     return NVFP4_ERR_CUDA;
   return launched();
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" {
+
+nvfp4_status moe_ffn_grouped(const uint16_t* x, int32_t m, int32_t top_k, const float* probs,
+                             const int32_t* expert_offsets, const int32_t* sorted_pairs,
+                             const nvfp4_weight* gate_up, const nvfp4_weight* down,
+                             const nvfp4_weight* shared_gate_up, const nvfp4_weight* shared_down, uint16_t* out,
+                             void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return moe_ffn_launch(x, m, top_k, probs, expert_offsets, sorted_pairs, gate_up, down, shared_gate_up, shared_down,
+                        out, ws, ws_bytes, stream);
+}
+
+nvfp4_status moe_forward(const uint16_t* x, const float* logits, int32_t m, int32_t top_k, int32_t route_flags,
+                         const float* expert_scale, int32_t* ids, float* probs, int32_t* expert_offsets,
+                         int32_t* sorted_pairs, const nvfp4_weight* gate_up, const nvfp4_weight* down,
+                         const nvfp4_weight* shared_gate_up, const nvfp4_weight* shared_down, uint16_t* out, void* ws,
+                         size_t ws_bytes, cudaStream_t stream) {
+  // both calls' arguments are checked before the first launch (the router's own
+  // checks cover logits, ids, offsets and pairs; the FFN's the rest)
+  if (!logits || !ids) return NVFP4_ERR_NULL;
+  if (const nvfp4_status st = moe_ffn_check(x, m, top_k, probs, expert_offsets, sorted_pairs, gate_up, down,
+                                            shared_gate_up, shared_down, out, ws, ws_bytes))
+    return st;
+  if (top_k > 32 || gate_up->num_matrices > 1024) return NVFP4_ERR_SHAPE;
+  if (const nvfp4_status st = moe_route_topk_ex(logits, m, gate_up->num_matrices, top_k, route_flags, expert_scale,
+                                                ids, probs, expert_offsets, sorted_pairs, stream))
+    return st;
+  return moe_ffn_launch(x, m, top_k, probs, expert_offsets, sorted_pairs, gate_up, down, shared_gate_up, shared_down,
+                        out, ws, ws_bytes, stream);
 }
 
 }  // extern "C"

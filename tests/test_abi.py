@@ -203,3 +203,26 @@ def test_w4a4_calls_reject_bad_arguments_before_launch(so):
     assert so.nvfp4_quantize_act(buf, 2, 60, buf, buf, buf, ws, 256, None) != 0            # k % 16
     assert so.nvfp4_quantize_act(buf, 5000, 64, buf, buf, buf, ws, 256, None) != 0         # m > 4096
     assert so.nvfp4_quantize_act(buf, 2, 64, buf, buf, buf, ws, 0, None) != 0              # workspace
+
+
+def test_moe_forward_checks_both_steps_before_launch(so):
+    """moe_forward returns the router's and the FFN's argument errors before its first
+    launch: a null logits or ids pointer, an FFN shape error, a bad top_k, a small
+    workspace."""
+    p = ctypes.c_void_p(1 << 20)
+    gu = _weight(n=1408, k=2816, e=128, flags=1)
+    dn = _weight(n=2816, k=704, e=128)
+    # x, logits, m, top_k, flags, scale, ids, probs, offsets, pairs, gate_up, down, sh_gu, sh_dn, out, ws, bytes, stream
+    args = [p, p, 15, 8, 0, None, p, p, p, p, ctypes.byref(gu), ctypes.byref(dn), None, None, p, p, 1 << 30, None]
+
+    def call(i, v):
+        bad = list(args)
+        bad[i] = v
+        return so.moe_forward(*bad)
+    assert call(1, None) == 1                                                  # null logits
+    assert call(6, None) == 1                                                  # null ids
+    assert call(0, None) == 1                                                  # null x
+    assert call(11, ctypes.byref(_weight(n=2816, k=704, e=64))) == 2          # expert count mismatch
+    assert call(3, 0) == 2                                                     # top_k < 1
+    assert call(3, 33) == 2                                                    # top_k > 32
+    assert call(16, 1024) == 4                                                 # workspace too small

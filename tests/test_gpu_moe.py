@@ -225,3 +225,25 @@ def test_moe_prefill_config4_full_size(lib):
     assert np.array_equal(pairs.cpu().numpy(), ref["sorted_pairs"])
     assert ref["counts"].max() > 32   # experts span several 32-pair blocks, the last one ragged
     assert lib.device_error() == 0
+
+
+@pytest.mark.parametrize("m", [1, 4, 15, 40])
+def test_moe_forward_equals_route_then_ffn(lib, m):
+    """moe_forward (one call) gives the same bytes as moe_route_topk followed by
+    moe_ffn_grouped, and the same routing, for decode batches and a prefill chunk."""
+    mc = W.MoECase(m=m, d=256, inter=128, n_experts=16, top_k=4, tag="forward")
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev())  # noqa: E731
+    gu = lib.prepare(up(np.stack([mc.gate_up(e) for e in range(16)])), gated=True)
+    dn = lib.prepare(up(np.stack([mc.down(e) for e in range(16)])))
+    sgu, sdn = lib.prepare(up(mc.gate_up(-1)), gated=True), lib.prepare(up(mc.down(-1)))
+    xb, _ = mc.x()
+    x = upload_bf16(xb)
+    logits = up(mc.logits())
+    ids, probs, offs, pairs = lib.route_topk(logits, 4)
+    ref = lib.moe_ffn(x, 4, probs, offs, pairs, gu, dn, sgu, sdn).clone()
+    out, (ids2, probs2, offs2, pairs2) = lib.moe_forward(x, logits, 4, gu, dn, sgu, sdn)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids2) and torch.equal(probs, probs2) and torch.equal(offs, offs2)
+    assert torch.equal(pairs, pairs2)
+    assert torch.equal(out, ref)
+    assert lib.device_error() == 0
