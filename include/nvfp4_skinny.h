@@ -38,6 +38,13 @@
  *     finite; router logits are finite or -inf (a NaN logit counts as -inf);
  *     expert ids passed to moe_ffn_grouped come from moe_route_topk;
  *     workspaces are not shared by calls that may run concurrently.
+ *   - The weight-streaming calls launch with programmatic dependent launch:
+ *     they start copying weights (data and global_scale) while the preceding
+ *     kernel on the stream may still run, and read activations only after it
+ *     has completed.  So a weight must be complete before the kernel just
+ *     before the call starts, or be written by a kernel that does not use
+ *     griddepcontrol.launch_dependents (nvfp4_quantize, nvfp4_repack and
+ *     ordinary library or framework kernels do not).
  *   - Kernel waits are bounded (about one second); a wait that runs out sets a
  *     bit in a device error word read by nvfp4_device_error().
  */
