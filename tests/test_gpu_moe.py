@@ -60,8 +60,11 @@ def test_moe_layer_with_weight_options(lib):
     and per-expert scales, for a decode batch and a prefill chunk."""
     scale = (0.5 + np.abs(W.normal_f32((8,), 77))).astype(np.float32)
     for m in (5, 40):
-        got, ref, _ = _moe_case(lib, m, 128, 64, 8, 3, True, "moe-small", softmax_all=True, expert_scale=scale)
-        check_bound(got, ref["out"], ref["tol_scale"], True, f"moe weight options m={m}")
+        for forward in (False, True):
+            got, ref, (ids, _, _) = _moe_case(lib, m, 128, 64, 8, 3, True, "moe-small", softmax_all=True,
+                                              expert_scale=scale, forward=forward)
+            assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+            check_bound(got, ref["out"], ref["tol_scale"], True, f"moe weight options m={m} forward={forward}")
     assert lib.device_error() == 0
 
 
@@ -135,10 +138,11 @@ def _experts(lib, case, shared):
 
 
 def _moe_case(lib, m, d, inter, n_exp, top_k, shared, tag, logits=None, rows=None, softmax_all=False,
-              expert_scale=None):
+              expert_scale=None, forward=False):
     """Run the layer on the GPU for all m tokens; the oracle computes the tokens in
     `rows` (all by default) -- a token's output depends on its own x and logits only.
-    Kernels and oracle use the same (oracle-quantized) weight bytes."""
+    Kernels and oracle use the same (oracle-quantized) weight bytes.  forward: the
+    one-call moe_forward instead of moe_route_topk_ex then moe_ffn_grouped."""
     case = W.MoECase(m=m, d=d, inter=inter, n_experts=n_exp, top_k=top_k, tag=tag)
     qgu, qdn, qsgu, qsdn, wgu, wdn, sgu, sdn = _experts(lib, case, shared)
     xb, xf = case.x()
@@ -146,9 +150,13 @@ def _moe_case(lib, m, d, inter, n_exp, top_k, shared, tag, logits=None, rows=Non
         logits = case.logits()
     x = upload_bf16(xb)
     scale_dev = upload_f32(expert_scale) if expert_scale is not None else None
-    ids, probs, offsets, pairs = lib.route_topk(upload_f32(logits), top_k, softmax_all=softmax_all,
-                                                expert_scale=scale_dev)
-    out = lib.moe_ffn(x, top_k, probs, offsets, pairs, wgu, wdn, sgu, sdn)
+    if forward:
+        out, (ids, probs, offsets, pairs) = lib.moe_forward(x, upload_f32(logits), top_k, wgu, wdn, sgu, sdn,
+                                                            softmax_all=softmax_all, expert_scale=scale_dev)
+    else:
+        ids, probs, offsets, pairs = lib.route_topk(upload_f32(logits), top_k, softmax_all=softmax_all,
+                                                    expert_scale=scale_dev)
+        out = lib.moe_ffn(x, top_k, probs, offsets, pairs, wgu, wdn, sgu, sdn)
     torch.cuda.synchronize()
     got = bf16_to_f64(out)
     if rows is not None:
@@ -158,14 +166,17 @@ def _moe_case(lib, m, d, inter, n_exp, top_k, shared, tag, logits=None, rows=Non
     return got, ref, (ids, offsets, pairs)
 
 
+@pytest.mark.parametrize("forward", [False, True])
 @pytest.mark.parametrize("m", [1, 2, 5, 8, 9, 15, 16, 17, 33, 64, 100])
 @pytest.mark.parametrize("shared", [True, False])
-def test_moe_small(lib, m, shared):
+def test_moe_small(lib, m, shared, forward):
     """m <= 16: one segment per expert; m > 16 (prefill): each expert's pairs in
-    blocks of 32, the last one ragged, and the shared expert in blocks of 32 tokens."""
-    got, ref, (ids, offsets, pairs) = _moe_case(lib, m, 128, 64, 8, 3, shared, "moe-small")
+    blocks of 32, the last one ragged, and the shared expert in blocks of 32 tokens.
+    Through moe_forward as well."""
+    got, ref, (ids, offsets, pairs) = _moe_case(lib, m, 128, 64, 8, 3, shared, "moe-small", forward=forward)
     assert np.array_equal(ids.cpu().numpy(), ref["ids"])
     assert np.array_equal(offsets.cpu().numpy(), ref["offsets"])
+    assert np.array_equal(pairs.cpu().numpy(), ref["sorted_pairs"])
     check_bound(got, ref["out"], ref["tol_scale"], True, f"moe small m={m} shared={shared}")
 
 
@@ -201,6 +212,19 @@ def test_moe_config2_full_size(lib, m):
     assert lib.device_error() == 0
 
 
+@pytest.mark.parametrize("m", [1, 15, 16])
+def test_moe_forward_config2_full_size(lib, m):
+    """The full-size layer through moe_forward: every output element against the
+    oracle, the routing bit-exact."""
+    got, ref, (ids, offsets, pairs) = _moe_case(lib, m, W.HIDDEN, W.INTER, W.N_EXPERTS, W.TOP_K, True, "moe",
+                                                forward=True)
+    check_bound(got, ref["out"], ref["tol_scale"], True, f"moe_forward config2 m={m}")
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    assert np.array_equal(offsets.cpu().numpy(), ref["offsets"])
+    assert np.array_equal(pairs.cpu().numpy(), ref["sorted_pairs"])
+    assert lib.device_error() == 0
+
+
 def test_moe_workspace_reused_across_shapes(lib):
     """One workspace serves calls of different m: a 15-token call fills h and the
     down outputs, then a 1-token call (which splits K and needs zeroed arrival
@@ -227,7 +251,7 @@ def test_moe_prefill_config4_full_size(lib):
     assert lib.device_error() == 0
 
 
-@pytest.mark.parametrize("m", [1, 4, 15, 40])
+@pytest.mark.parametrize("m", [1, 2, 4, 8, 15, 16, 40])
 def test_moe_forward_equals_route_then_ffn(lib, m):
     """moe_forward (one call) gives the same bytes as moe_route_topk followed by
     moe_ffn_grouped, and the same routing, for decode batches and a prefill chunk."""
@@ -246,4 +270,34 @@ def test_moe_forward_equals_route_then_ffn(lib, m):
     assert torch.equal(ids, ids2) and torch.equal(probs, probs2) and torch.equal(offs, offs2)
     assert torch.equal(pairs, pairs2)
     assert torch.equal(out, ref)
+    assert lib.device_error() == 0
+
+
+def test_moe_forward_special_logits_and_options(lib):
+    """moe_forward on NaN / -inf logits (a NaN counts as -inf; an all-NaN token gets
+    weight 0) and with the softmax over all experts and per-expert scales: the same
+    routing and bytes as moe_route_topk_ex followed by moe_ffn_grouped."""
+    m, e, k = 6, 16, 4
+    mc = W.MoECase(m=m, d=256, inter=128, n_experts=e, top_k=k, tag="forward-special")
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev())  # noqa: E731
+    gu = lib.prepare(up(np.stack([mc.gate_up(i) for i in range(e)])), gated=True)
+    dn = lib.prepare(up(np.stack([mc.down(i) for i in range(e)])))
+    xb, _ = mc.x()
+    x = upload_bf16(xb)
+    lg = mc.logits().copy()
+    lg[0, [1, 5, 9]] = np.nan
+    lg[1, 3:] = -np.inf
+    lg[2, :] = np.nan
+    lg[3, ::2] = -np.inf
+    logits = up(lg)
+    scale = up(0.5 + np.abs(W.normal_f32((e,), 91)))
+    for softmax_all, es in ((False, None), (True, None), (False, scale), (True, scale)):
+        ids, probs, offs, pairs = lib.route_topk(logits, k, softmax_all=softmax_all, expert_scale=es)
+        ref = lib.moe_ffn(x, k, probs, offs, pairs, gu, dn).clone()
+        out, (ids2, probs2, offs2, pairs2) = lib.moe_forward(x, logits, k, gu, dn, softmax_all=softmax_all,
+                                                             expert_scale=es)
+        torch.cuda.synchronize()
+        assert torch.equal(ids, ids2) and torch.equal(offs, offs2) and torch.equal(pairs, pairs2)
+        assert torch.equal(probs, probs2)
+        assert torch.equal(out, ref)
     assert lib.device_error() == 0
