@@ -123,6 +123,17 @@ uint32_t nvfp4_layout_version(void);
  */
 nvfp4_status nvfp4_device_error(uint32_t *out, int32_t clear);
 
+/*
+ * Self-test of the failure path of the bounded waits (no fault, no hang):
+ * launches one CTA whose warps wait, with the kernels' own bounded
+ * warp-collective wait, on an mbarrier phase that nothing completes, and give
+ * up after limit_cycles SM clock cycles (1 .. 2^31) instead of the kernels'
+ * ~1 s.  The kernel then sets bit 0 of the device error word and returns; the
+ * context stays usable.  Asynchronous on `stream`; read the word with
+ * nvfp4_device_error afterwards.  NVFP4_ERR_SHAPE for a limit out of range.
+ */
+nvfp4_status nvfp4_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream);
+
 /* Bytes of a repacked weight of num_matrices x [n, k] (0 for invalid sizes). */
 size_t nvfp4_repacked_bytes(int32_t n, int32_t k, int32_t num_matrices);
 

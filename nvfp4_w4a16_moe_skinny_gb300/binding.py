@@ -29,7 +29,7 @@ EXPORTS = (
     "nvfp4_gemm", "moe_route_topk", "moe_ffn_workspace_bytes", "moe_ffn_grouped",
     "lm_head_workspace_bytes", "lm_head_argmax", "lm_head_argmax_noalloc", "nvfp4_plan_info",
     "lm_head_sample", "moe_route_topk_ex", "lm_head_sample_ex", "nvfp4_plan_check", "moe_router_logits",
-    "nvfp4_repack_host", "nvfp4_quantize_act", "nvfp4_gemm_w4a4", "lm_head_argmax_w4a4", "moe_forward",
+    "nvfp4_repack_host", "nvfp4_quantize_act", "nvfp4_gemm_w4a4", "lm_head_argmax_w4a4", "moe_forward", "nvfp4_selftest_wait_timeout",
 )
 
 
@@ -111,6 +111,8 @@ def _sig(lib):
                                 ctypes.POINTER(CWeight), ctypes.POINTER(CWeight), ctypes.POINTER(CWeight), _P, _P, _SZ,
                                 _P]
     lib.moe_forward.restype = ctypes.c_int
+    lib.nvfp4_selftest_wait_timeout.argtypes = [ctypes.c_int64, _P]
+    lib.nvfp4_selftest_wait_timeout.restype = ctypes.c_int
     lib.nvfp4_quantize_act.argtypes = [_P, _I, _I, _P, _P, _P, _P, _SZ, _P]
     lib.nvfp4_quantize_act.restype = ctypes.c_int
     lib.nvfp4_gemm_w4a4.argtypes = [ctypes.POINTER(CWeight), _P, _P, _P, _I, _P, _P, _SZ, _P]
@@ -163,6 +165,11 @@ class Library:
         v = ctypes.c_uint32(0)
         self._check("nvfp4_device_error", self.lib.nvfp4_device_error(ctypes.byref(v), int(clear)))
         return v.value
+
+    def selftest_wait_timeout(self, limit_cycles: int, stream=None):
+        """Run the bounded-wait self-test (a wait that runs out after limit_cycles)."""
+        self._check("nvfp4_selftest_wait_timeout", self.lib.nvfp4_selftest_wait_timeout(int(limit_cycles),
+                                                                                        _stream(stream)))
 
     def repacked_bytes(self, n, k, num_matrices=1) -> int:
         return self.lib.nvfp4_repacked_bytes(n, k, num_matrices)

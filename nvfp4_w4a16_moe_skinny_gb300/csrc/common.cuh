@@ -113,31 +113,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Bounded wait of one thread for the phase with the given parity to complete:
-// false, with kErrWaitTimeout recorded, if it did not within kWaitCycles.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  const long long t0 = clock64();
-  while (!mbar_try_wait_sleep(bar, parity, 1u << 20)) {
-    if (clock64() - t0 > kWaitCycles) {
-      atomicOr(&g_device_error, kErrWaitTimeout);
-      return false;
-    }
-  }
-  return true;
-}
-
 // Bounded warp-collective wait (all 32 lanes call it) for the phase with the
 // given parity to complete.  Every lane observes the completion itself (so the
 // bulk-copied bytes are visible to it) and all lanes return the same answer:
 // false, with kErrWaitTimeout recorded, if the phase did not complete within
-// kWaitCycles.  The first probe does not suspend: a stage is usually full
-// already.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
+// `limit` SM clock cycles (the kernels: kWaitCycles).  The first probe does not
+// suspend: a stage is usually full already.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, long long limit = kWaitCycles) {
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   const long long t0 = clock64();
   while (true) {
     if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, 1u << 20))) return true;
-    if (__any_sync(0xffffffffu, clock64() - t0 > kWaitCycles)) {
+    if (__any_sync(0xffffffffu, clock64() - t0 > limit)) {
       if ((threadIdx.x & 31) == 0) atomicOr(&g_device_error, kErrWaitTimeout);
       return false;
     }

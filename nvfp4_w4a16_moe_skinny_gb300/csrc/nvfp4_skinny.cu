@@ -311,6 +311,20 @@ int dense_split(int m, int n, int k) {
   return choose_split(m, ceil_div(n, kGroupRows), ceil_div(k, kTileK), 1, 1, 0, false, false, true);
 }
 
+// The failure path of the bounded waits, without a fault: every warp of one CTA
+// waits, with the kernels' warp-collective wait, on an mbarrier phase that no
+// thread completes (no copy is attached to it), gives up after `limit` cycles,
+// records kErrWaitTimeout and returns.
+__global__ void __launch_bounds__(128) selftest_wait_kernel(long long limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  (void)mbar_wait_warp(&bar, 0, limit);
+}
+
 }  // namespace
 }  // namespace nvfp4
 
@@ -332,6 +346,12 @@ const char* nvfp4_status_string(nvfp4_status st) {
 }
 
 uint32_t nvfp4_layout_version(void) { return NVFP4_LAYOUT_VERSION; }
+
+nvfp4_status nvfp4_selftest_wait_timeout(int64_t limit_cycles, cudaStream_t stream) {
+  if (limit_cycles < 1 || limit_cycles > (int64_t{1} << 31)) return NVFP4_ERR_SHAPE;
+  selftest_wait_kernel<<<1, 128, 0, stream>>>(static_cast<long long>(limit_cycles));
+  return launched();
+}
 
 nvfp4_status nvfp4_device_error(uint32_t* out, int32_t clear) {
   if (!out) return NVFP4_ERR_NULL;

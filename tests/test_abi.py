@@ -226,3 +226,9 @@ def test_moe_forward_checks_both_steps_before_launch(so):
     assert call(3, 0) == 2                                                     # top_k < 1
     assert call(3, 33) == 2                                                    # top_k > 32
     assert call(16, 1024) == 4                                                 # workspace too small
+
+
+def test_selftest_rejects_a_limit_out_of_range_before_launch(so):
+    assert so.nvfp4_selftest_wait_timeout(0, None) == 2
+    assert so.nvfp4_selftest_wait_timeout(-5, None) == 2
+    assert so.nvfp4_selftest_wait_timeout((1 << 31) + 1, None) == 2
