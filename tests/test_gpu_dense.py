@@ -150,6 +150,15 @@ def test_gemm_ragged_all_m(lib, m, n, k):
     check_bound(got, exact, absy, True, f"gemm m={m} n={n} k={k}")
 
 
+@pytest.mark.parametrize("m,n,k", [(1, 512, 16384), (16, 512, 16384), (7, 1000, 12288), (3, 136, 32768)])
+def test_gemm_long_k(lib, m, n, k):
+    """Long rows: the planner splits K 10-16 ways (five rounds of partials per tile at
+    M=16), a 32,768-column row at M=3, a ragged N at M=7."""
+    got, exact, absy = _dense(lib, m, n, k, 3000 + n + k, 4000 + m)
+    check_bound(got, exact, absy, True, f"gemm long k m={m} n={n} k={k}")
+    assert lib.device_error() == 0
+
+
 def _wide_range_case(m, n, k, small_exp, big_cols_weight):
     """x rows with 2^10 at every 64th column and +-2^small_exp * (1 + j/128) elsewhere;
     the weight's columns under the large values are zero unless big_cols_weight."""

@@ -301,3 +301,19 @@ def test_moe_forward_special_logits_and_options(lib):
         assert torch.equal(probs, probs2)
         assert torch.equal(out, ref)
     assert lib.device_error() == 0
+
+
+@pytest.mark.parametrize("m,n_exp,top_k,d,inter", [(16, 1024, 32, 128, 64), (1, 1024, 32, 256, 128),
+                                                   (16, 512, 16, 128, 64)])
+@pytest.mark.parametrize("forward", [False, True])
+def test_moe_many_experts(lib, m, n_exp, top_k, d, inter, forward):
+    """Decode batches routed over many experts: up to 512 pairs over 1,024 experts (513
+    segments with the shared expert, several per CTA), top-32 routing with the widest
+    router instance, against the oracle element by element and the grouping bit-exact."""
+    got, ref, (ids, offsets, pairs) = _moe_case(lib, m, d, inter, n_exp, top_k, True, "moe-many", forward=forward)
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    assert np.array_equal(offsets.cpu().numpy(), ref["offsets"])
+    assert np.array_equal(pairs.cpu().numpy(), ref["sorted_pairs"])
+    assert (np.diff(ref["offsets"]) > 0).sum() > min(n_exp, m * top_k) // 2  # many active experts
+    check_bound(got, ref["out"], ref["tol_scale"], True, f"moe many experts m={m} e={n_exp} k={top_k}")
+    assert lib.device_error() == 0
