@@ -142,6 +142,9 @@ def test_lm_head_and_moe_argument_errors(so):
     bad = list(args)
     bad[12] = 1024                                                          # workspace too small
     assert so.moe_ffn_grouped(*bad) == 4
+    bad = list(args)                                                        # d and I must be multiples of 64
+    bad[6], bad[7] = ctypes.byref(_weight(n=192, k=208, e=128, flags=1)), ctypes.byref(_weight(n=208, k=96, e=128))
+    assert so.moe_ffn_grouped(*bad) == 2
 
 
 def test_binding_refuses_to_run_without_the_library(tmp_path):

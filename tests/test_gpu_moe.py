@@ -317,3 +317,17 @@ def test_moe_many_experts(lib, m, n_exp, top_k, d, inter, forward):
     assert (np.diff(ref["offsets"]) > 0).sum() > min(n_exp, m * top_k) // 2  # many active experts
     check_bound(got, ref["out"], ref["tol_scale"], True, f"moe many experts m={m} e={n_exp} k={top_k}")
     assert lib.device_error() == 0
+
+
+@pytest.mark.parametrize("m", [1, 5, 16, 40])
+@pytest.mark.parametrize("forward", [False, True])
+def test_moe_odd_chunk_counts(lib, m, forward):
+    """Odd chunk and group counts (the MoE calls take d and I in multiples of 64):
+    d = 320 (five 64-column chunks for gate+up, five 64-row groups for down) and
+    I = 192 (three chunks for down, six gated groups), decode batches and a prefill
+    chunk."""
+    got, ref, (ids, offsets, pairs) = _moe_case(lib, m, 320, 192, 8, 3, True, "moe-odd", forward=forward)
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    assert np.array_equal(offsets.cpu().numpy(), ref["offsets"])
+    check_bound(got, ref["out"], ref["tol_scale"], True, f"moe odd chunk counts m={m}")
+    assert lib.device_error() == 0
