@@ -331,3 +331,16 @@ def test_moe_odd_chunk_counts(lib, m, forward):
     assert np.array_equal(offsets.cpu().numpy(), ref["offsets"])
     check_bound(got, ref["out"], ref["tol_scale"], True, f"moe odd chunk counts m={m}")
     assert lib.device_error() == 0
+
+
+@pytest.mark.parametrize("m,top_k,n_exp", [(2048, 8, 128), (4096, 4, 128), (4096, 4, 16)])
+def test_moe_prefill_max_pairs(lib, m, top_k, n_exp):
+    """Prefill chunks at the calls' limit of 16,384 (token, slot) pairs, over 128 experts
+    (about 128 pairs each) and over 16 (about 1,024 each, 32 blocks per expert): every
+    token against the oracle, the grouping bit-exact."""
+    got, ref, (ids, offsets, pairs) = _moe_case(lib, m, 128, 64, n_exp, top_k, True, "moe-max")
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    assert np.array_equal(offsets.cpu().numpy(), ref["offsets"])
+    assert np.array_equal(pairs.cpu().numpy(), ref["sorted_pairs"])
+    check_bound(got, ref["out"], ref["tol_scale"], True, f"moe prefill max pairs m={m} k={top_k} e={n_exp}")
+    assert lib.device_error() == 0
