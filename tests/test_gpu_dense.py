@@ -275,7 +275,7 @@ def _check_argmax(mx, idx, ref, parts, what):
 
 
 @pytest.mark.parametrize("m", [1, 3, 7, 8, 15, 16])
-@pytest.mark.parametrize("vocab,k", [(3000, 256), (1037, 2816)])
+@pytest.mark.parametrize("vocab,k", [(3000, 256), (1037, 2816), (1, 64), (17, 16), (64, 4096)])
 def test_lm_head_small(lib, m, vocab, k):
     mx, idx, ref, parts = _lm(lib, m, vocab, k, 300 + vocab, 400 + m)
     _check_argmax(mx, idx, ref, parts, f"lm_head m={m} vocab={vocab}")
