@@ -335,9 +335,11 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
 }
 
 // float -> f16 bits, round to nearest even.
-__device__ __forceinline__ uint16_t f32_to_f16_bits(float f) {
-  uint16_t r;
-  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(f));
+// Two floats to an f16x2 (lo in the low half), each rounded to nearest even, in
+// one conversion.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 

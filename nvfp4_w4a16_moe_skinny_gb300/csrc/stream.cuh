@@ -215,7 +215,7 @@ __device__ __forceinline__ void stage_rows(const uint16_t* __restrict__ x, int k
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float lo = __uint_as_float(w4[e] << 16) * sc, hi = __uint_as_float(w4[e] & 0xFFFF0000u) * sc;
-      h[e] = static_cast<uint32_t>(f32_to_f16_bits(lo)) | (static_cast<uint32_t>(f32_to_f16_bits(hi)) << 16);
+      h[e] = f32x2_to_f16x2(lo, hi);
     }
     place8<kMMA>(rowp, c8, h);
   };
