@@ -334,7 +334,6 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   return r;
 }
 
-// float -> f16 bits, round to nearest even.
 // Two floats to an f16x2 (lo in the low half), each rounded to nearest even, in
 // one conversion.
 __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
