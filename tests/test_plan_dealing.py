@@ -98,7 +98,8 @@ def segments(counts, m, shared=True):
 
 
 @pytest.mark.parametrize("sms", [152, 148, 16])
-@pytest.mark.parametrize("n,k", [(4096, 4096), (14336, 4096), (512, 256), (1000, 320), (40, 80), (64, 1024)])
+@pytest.mark.parametrize("n,k", [(4096, 4096), (14336, 4096), (512, 256), (1000, 320), (40, 80), (64, 1024),
+                                 (512, 16384), (136, 32768), (1000, 12288)])
 def test_dense_plans_cover_every_tile_once(so, sms, n, k):
     for m in (1, 2, 4, 7, 8, 15, 16):
         check(so, 0, m, n, k, 1, sms=sms)
@@ -131,7 +132,9 @@ def test_busiest_warp_report(so):
 
 @pytest.mark.parametrize("m,top_k,n_exp,d,inter", [
     (1, 8, 128, 2816, 704), (15, 8, 128, 2816, 704), (16, 8, 128, 2816, 704), (512, 8, 128, 2816, 704),
-    (2, 3, 8, 128, 64), (16, 2, 6, 192, 128), (40, 3, 8, 128, 64), (100, 1, 40, 192, 128), (17, 2, 6, 192, 128)])
+    (2, 3, 8, 128, 64), (16, 2, 6, 192, 128), (40, 3, 8, 128, 64), (100, 1, 40, 192, 128), (17, 2, 6, 192, 128),
+    (16, 32, 1024, 128, 64), (1, 32, 1024, 256, 128), (16, 16, 512, 128, 64), (16, 3, 8, 320, 192),
+    (2048, 8, 128, 128, 64), (4096, 4, 16, 128, 64)])
 @pytest.mark.parametrize("sms", [152, 148, 16])
 def test_moe_plans_cover_every_tile_once(so, m, top_k, n_exp, d, inter, sms):
     for i, counts in enumerate(routings(m, top_k, n_exp, 7 * m + top_k)):
